@@ -1,0 +1,352 @@
+"""Benchmark of the GB300 attention forward (prints one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: the lecture demo's sequence-length sweep, non-causal MHA,
+B=4, H=8, D=64, Lq=Lk in {64, ..., 8192}.  One step = one forward pass at every
+length of the sweep.  `value` = total algorithmic FLOPs (4*B*H*Lq*Lk*D) of a
+step / device time of the step, in TFLOPS, with the inputs resident in HBM;
+L2 is flushed (a 256 MiB write) before every launch and the flush is not
+timed.  `e2e` is the same metric through the host-buffer API (pinned host
+tensors copied in, O and LSE copied back, inside the timed region).
+`per_config` adds the causal prefill, long-context and single-query decode
+workloads (device time, TFLOPS or GB/s, and the fraction of the measured
+peak).  `--impl reference` times the fp64 CPU oracle on a bounded sample of
+the same workload instead.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own
+GPU (heads are independent: weak scaling, no collective on the data path);
+rank 0 reports the max step time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (bf16) and % of GB300 BF16 peak; decode GB/s vs HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sweep_workloads():
+    from exact_attention_03_gb300.inputs import SWEEP_LENGTHS, sweep
+    return [sweep(L) for L in SWEEP_LENGTHS]
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def _time_launches(calls, flush, reps):
+    """Device time (ms) of each call, L2 flushed before each (not timed)."""
+    import torch
+    s = torch.cuda.current_stream()
+    evs = []
+    for _ in range(reps):
+        for fn in calls:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            fn()
+            e1.record(s)
+            evs.append((e0, e1))
+    s.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args, rank, world):
+    import torch
+    import exact_attention_03_gb300 as fa
+    from exact_attention_03_gb300 import build as fa_build
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+
+    fa_build.build()
+    fa.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def check():
+        st, site = fa.last_device_error()
+        if st != fa.FA_OK:
+            raise RuntimeError(f"device wait gave up: {st} at site {site}")
+
+    # ---- headline: the sweep, inputs resident in HBM
+    ws = sweep_workloads()
+    bufs = []
+    for w in ws:
+        q, k, v = make_inputs(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
+        bufs.append((w, q, k, v, o, lse))
+    calls = [(lambda w=w, q=q, k=k, v=v, o=o, lse=lse:
+              fa.forward(q, k, v, causal=w.causal, out=o, lse=lse)) for (w, q, k, v, o, lse) in bufs]
+    _time_launches(calls, flush, args.warmup)
+    check()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    t0 = time.perf_counter()
+    times = _time_launches(calls, flush, args.steps)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    check()
+    n = len(calls)
+    step_ms = [sum(times[i * n:(i + 1) * n]) for i in range(args.steps)]
+    mean_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([mean_step], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_step = float(t.item())
+    step_flops = sum(w.flops for w in ws)
+    value = world * step_flops / (mean_step * 1e-3) / 1e12
+    per_len = {}
+    for i, w in enumerate(ws):
+        ts = [times[s * n + i] for s in range(args.steps)]
+        ms = statistics.median(ts)
+        per_len[str(w.Lq)] = {"ms": round(ms, 5), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}
+
+    # ---- e2e: the same sweep through the host-buffer API
+    host = [(w, *(t.cpu().pin_memory() for t in (q, k, v))) for (w, q, k, v, _, _) in bufs]
+    for (w, qh, kh, vh) in host:
+        fa.forward_host(qh, kh, vh, causal=w.causal)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        s = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        flush.zero_()
+        e0.record(s)
+        for (w, qh, kh, vh) in host:
+            fa.forward_host(qh, kh, vh, causal=w.causal)
+        e1.record(s)
+        s.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    check()
+    h2d = sum(t.numel() * t.element_size() for (_, qh, kh, vh) in host for t in (qh, kh, vh))
+    d2h = sum(w.B * w.H * w.Lq * (w.D * 2 + 4) for w in ws)
+    e2e_value = world * step_flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q, k, v)",
+        "config": {"workload": "sweep_d64: non-causal MHA B=4 H=8 D=64, Lq=Lk in 64..8192 "
+                               "(one forward per length per step)",
+                   "global_batch": 4 * world, "seq_len": "64..8192",
+                   "l2": "flushed before every launch (256 MiB write, untimed)",
+                   "parallelism": f"replicas x{world} (heads independent)"},
+        "per_length": per_len,
+        "gpu_launches": n * args.steps,
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 3), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+    }
+    prefill_ms = mean_step  # every launch of the step is the prefill kernel
+    achieved = step_flops / (prefill_ms * 1e-3) / 1e12
+    result["roofline"] = {"kernel": "fa_prefill_kernel<64>", "bound": "tensor",
+                          "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
+                          "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                          "peak_source": f"{peak_src} bf16 burst", "traffic": None}
+    del bufs, calls, host
+
+    if rank == 0 and world == 1 and not args.no_configs:
+        result["per_config"] = per_config(args, fa, flush, dev, peaks, check)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return result
+
+
+def per_config(args, fa, flush, dev, peaks, check):
+    import torch
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+    out = {}
+    for name, reps in (("mha_l256_d64", 20), ("causal_l8k_d128", 10),
+                       ("causal_l64k_d128", 3), ("decode_l128k_d128", 5)):
+        w = WORKLOADS[name]
+        q, k, v = make_inputs(w, dev)
+        o = torch.empty((w.B, w.H, w.Lq, w.D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
+        call = lambda: fa.forward(q, k, v, causal=w.causal, out=o, lse=lse)
+        _time_launches([call], flush, 2)
+        ts = _time_launches([call], flush, reps)
+        check()
+        ms = statistics.median(ts)
+        entry = {"B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "D": w.D, "causal": w.causal,
+                 "ms": round(ms, 5)}
+        if w.Lq == 1:
+            gbs = w.bytes / (ms * 1e-3) / 1e9
+            entry.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                          "launches": 2})
+        else:
+            tf = w.flops / (ms * 1e-3) / 1e12
+            entry.update({"TFLOPS": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+                          "launches": 1})
+        out[name] = entry
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def _oracle_sample(max_seconds, per_len_rows=None):
+    """Runs the oracle on a bounded sample of the sweep; returns (flops, seconds, desc)."""
+    import numpy as np
+    from exact_attention_03_gb300.inputs import make_inputs
+    from oracle.naive import attention_head, to_f64
+
+    flops = 0.0
+    spent = 0.0
+    parts = []
+    for w in sweep_workloads():
+        q, k, v = make_inputs(w.with_(B=1), "cpu")
+        qh, kh, vh = to_f64(q[0, 0]), to_f64(k[0, 0]), to_f64(v[0, 0])
+        rows = w.Lq if per_len_rows is None else min(w.Lq, per_len_rows)
+        t0 = time.perf_counter()
+        attention_head(qh, kh, vh, w.scale, causal=w.causal, rows=np.arange(rows))
+        spent += time.perf_counter() - t0
+        flops += 4.0 * rows * w.Lk * w.D
+        parts.append(f"L={w.Lq}:{rows} rows")
+        if spent > max_seconds:
+            break
+    return flops, spent, "head (b=0,h=0) of each sweep length, " + ", ".join(parts)
+
+
+def cpu_baseline(seconds):
+    flops, spent, desc = _oracle_sample(seconds)
+    return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOPS",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": desc + " (numpy fp64, BLAS threads = all host cores)",
+            "seconds": round(spent, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    step = []
+    for i in range(args.warmup + args.steps):
+        flops, spent, desc = _oracle_sample(1e9, per_len_rows=128)
+        if i >= args.warmup:
+            step.append((flops, spent))
+    flops = sum(f for f, _ in step)
+    secs = sum(s for _, s in step)
+    value = flops / secs / 1e12
+    cores = len(os.sched_getaffinity(0))
+    return {"metric": METRIC, "impl": "reference", "value": round(value, 6), "unit": "TFLOPS",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / len(step) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "sweep_d64: non-causal MHA B=4 H=8 D=64, Lq=Lk in 64..8192",
+                       "sample": desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config section")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,165 @@
+"""GB300 (sm_103a) exact-attention forward: thin Python binding of libfa_gb300.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+only marshals arguments (pointers, sizes, the current CUDA stream) through the
+C ABI declared in include/fa.h.  PyTorch is used for device memory and
+streams.  There is no fallback: if the library is missing, or the call fails,
+an exception is raised.
+
+    import exact_attention_03_gb300 as fa
+    o, lse = fa.forward(q, k, v, causal=True)          # bf16 [B,H,L,D] on cuda
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+__all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
+           "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
+           "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
+           "forward", "forward_host", "EXPORTED_SYMBOLS"]
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = -1
+FA_ERR_UNSUPPORTED = -2
+FA_ERR_MISALIGNED = -3
+FA_ERR_CUDA = -4
+FA_ERR_TIMEOUT = -5
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libfa_gb300.so"
+_lib = None
+
+# name -> (restype, argtypes)
+_SIGS = {
+    "fa_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                              ctypes.c_void_p]),
+    "fa_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa_last_device_error": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]),
+    "fa_decode_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "fa_wait_selftest": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
+    "fa_abi_version": (ctypes.c_int, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGS)
+
+
+class FlashAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str = "fa_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {status} ({strerror(status)})")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, _LIB_NAME)
+
+
+def load():
+    """Loads the CUDA library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: build it with exact_attention_03_gb300.build.build()")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load().fa_strerror(int(status)).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Lq, Lk, D, scale, causal, stream) -> int:
+    """Raw C-ABI call: integer pointers / sizes in, status code out."""
+    return load().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Lq, Lk, D,
+                         float(scale), int(causal), stream)
+
+
+def last_device_error(stream=None) -> Tuple[int, int]:
+    """(status, wait site) of the device error word; synchronises `stream`."""
+    site = ctypes.c_int(0)
+    st = load().fa_last_device_error(_stream_handle(stream), ctypes.byref(site))
+    return st, site.value
+
+
+def wait_selftest(limit_us: int = 20000, stream=None) -> int:
+    return load().fa_wait_selftest(int(limit_us), _stream_handle(stream))
+
+
+def decode_num_splits(BH: int, Lk: int, num_sms: int) -> int:
+    return load().fa_decode_num_splits(int(BH), int(Lk), int(num_sms))
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        stream = torch.cuda.current_stream()
+    if hasattr(stream, "cuda_stream"):
+        return stream.cuda_stream
+    return stream
+
+
+def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None,
+            lse=None, return_lse: bool = True, stream=None):
+    """O (bf16 [B,H,Lq,D]) and LSE (fp32 [B,H,Lq]) for CUDA bf16 q [B,H,Lq,D],
+    k, v [B,H,Lk,D].  `scale` defaults to 1/sqrt(D)."""
+    import torch
+
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, L, D]")
+    B, H, Lq, D = q.shape
+    if k.shape != (B, H, k.shape[2], D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA bf16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                lse.data_ptr() if lse is not None else None, B, H, Lq, Lk, D, scale,
+                int(causal), _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st)
+    return out, lse
+
+
+def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None,
+                 device="cuda", stream=None):
+    """End-to-end call on host tensors: copies q, k, v (pinned CPU bf16) to the
+    device, runs the forward pass and copies O and LSE back into pinned host
+    tensors.  Returns (O, LSE) on the host after synchronising the stream."""
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    with torch.cuda.stream(s):
+        qd = q.to(device, non_blocking=True)
+        kd = k.to(device, non_blocking=True)
+        vd = v.to(device, non_blocking=True)
+        o, lse = forward(qd, kd, vd, causal=causal, scale=scale, stream=s)
+        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+    s.synchronize()
+    return oh, lh

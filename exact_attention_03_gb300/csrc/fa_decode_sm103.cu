@@ -1,0 +1,245 @@
+// fa_decode_sm103.cu - single-query (Lq == 1) attention: split-K/V + combine.
+//
+// With one query row per head a tensor-core tile would be 1/128 full and the
+// work is a pure stream over K and V (about 1 flop per byte), so it runs on
+// CUDA cores and is sized for HBM bandwidth:
+//
+//   fa_decode_split_kernel  grid = B*H*n_split CTAs of 256 threads.  CTA
+//     (head, split) streams keys [split*chunk, (split+1)*chunk) of that head.
+//     A group of D/8 lanes owns one key at a time (16 bytes of K and of V per
+//     lane, coalesced 128/256-byte rows); each lane keeps several keys' K and
+//     V in flight.  The dot product is reduced with warp shuffles, then the
+//     group applies the guide's recurrence for its keys ("Expand: why
+//     multiplying by exp(d1 - d2) fixes it" / "Expand: the correction for the
+//     output O", NTU Hung-yi Lee ML 2026 Guide, quidproquo.cc): new max,
+//     rescale of the running denominator and output by 2^(m_old - m_new),
+//     add the new terms.  The CTA's groups are merged the same way through
+//     shared memory and the split writes (m, l, unnormalised O) in fp32.
+//   fa_decode_combine_kernel  one warp per head merges the n_split partials
+//     with the same rescale identity (M = max m_s, l = sum l_s 2^(m_s - M),
+//     O = sum O_s 2^(m_s - M) / l) and writes O (bf16) and LSE (fp32).
+// Exponentials are base 2: x = q.k * scale * log2(e).
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kUnroll = 4;  // keys per group kept in flight
+constexpr float kLn2 = 0.69314718055994530942f;
+
+struct DecParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;
+  float* lse;
+  float* part_o;   // [n_split][BH][D]
+  float* part_ml;  // [n_split][BH][2]  (m in log2 units, l)
+  int BH, Lk, n_split, chunk;
+  float scale_log2;
+};
+
+__device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr));
+  return r;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecParams p) {
+  constexpr int G = D / 8;             // lanes per key
+  constexpr int GPW = 32 / G;          // key groups per warp
+  constexpr int NG = kDecWarps * GPW;  // key groups per CTA
+  __shared__ float sm_m[NG], sm_l[NG];
+  __shared__ float sm_acc[NG][D];
+
+  const int split = int(blockIdx.x) % p.n_split;
+  const int bh = int(blockIdx.x) / p.n_split;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = warp * GPW + lane / G;  // key group of this lane
+  const int li = lane % G;               // this lane covers dims [8*li, 8*li + 8)
+
+  // query slice, pre-multiplied by scale*log2(e)
+  float qf[8];
+  {
+    const uint4 qw = *reinterpret_cast<const uint4*>(p.q + size_t(bh) * D + 8 * li);
+    const uint32_t w[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[2 * e] = bf_lo(w[e]) * p.scale_log2;
+      qf[2 * e + 1] = bf_hi(w[e]) * p.scale_log2;
+    }
+  }
+
+  const size_t head = size_t(bh) * size_t(p.Lk) * D;
+  const __nv_bfloat16* kp = p.k + head + 8 * li;
+  const __nv_bfloat16* vp = p.v + head + 8 * li;
+  const int kbeg = split * p.chunk;
+  const int kend = min(kbeg + p.chunk, p.Lk);
+
+  float m = -INFINITY, l = 0.f, acc[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+
+  // the loop bound is uniform over the CTA, so every lane takes part in the shuffles
+  for (int base = kbeg; base < kend; base += NG * kUnroll) {
+    uint4 kr[kUnroll], vr[kUnroll];
+    bool valid[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int key = base + u * NG + gi;
+      valid[u] = key < kend;
+      if (valid[u]) {
+        kr[u] = ld_stream16(kp + size_t(key) * D);
+        vr[u] = ld_stream16(vp + size_t(key) * D);
+      } else {
+        kr[u] = make_uint4(0, 0, 0, 0);
+        vr[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t w[4] = {kr[u].x, kr[u].y, kr[u].z, kr[u].w};
+      float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        d0 = fmaf(qf[2 * e], bf_lo(w[e]), d0);
+        d1 = fmaf(qf[2 * e + 1], bf_hi(w[e]), d1);
+      }
+      float d = d0 + d1;
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+      x[u] = valid[u] ? d : -INFINITY;
+    }
+    float mx = x[0];
+#pragma unroll
+    for (int u = 1; u < kUnroll; ++u) mx = fmaxf(mx, x[u]);
+    const float m_new = fmaxf(m, mx);
+    const float m_safe = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2_approx(m - m_safe);
+    l *= alpha;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] *= alpha;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const float pu = ex2_approx(x[u] - m_safe);
+      l += pu;
+      const uint32_t w[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[2 * e] = fmaf(pu, bf_lo(w[e]), acc[2 * e]);
+        acc[2 * e + 1] = fmaf(pu, bf_hi(w[e]), acc[2 * e + 1]);
+      }
+    }
+    m = m_new;
+  }
+
+  // merge the CTA's key groups
+  if (li == 0) {
+    sm_m[gi] = m;
+    sm_l[gi] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < 8; ++e) sm_acc[gi][8 * li + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    const int d = threadIdx.x;
+    float M = -INFINITY;
+#pragma unroll
+    for (int g2 = 0; g2 < NG; ++g2) M = fmaxf(M, sm_m[g2]);
+    const float M_safe = (M == -INFINITY) ? 0.f : M;
+    float od = 0.f, L = 0.f;
+#pragma unroll
+    for (int g2 = 0; g2 < NG; ++g2) {
+      const float w = ex2_approx(sm_m[g2] - M_safe);
+      od = fmaf(sm_acc[g2][d], w, od);
+      L = fmaf(sm_l[g2], w, L);
+    }
+    const size_t slot = size_t(split) * p.BH + bh;
+    p.part_o[slot * D + d] = od;
+    if (d == 0) {
+      p.part_ml[slot * 2 + 0] = M;
+      p.part_ml[slot * 2 + 1] = L;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecParams p) {
+  constexpr int E = D / 32;  // output dims per lane
+  const int bh = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (bh >= p.BH) return;
+
+  float M = -INFINITY;
+  for (int s = lane; s < p.n_split; s += 32) M = fmaxf(M, p.part_ml[(size_t(s) * p.BH + bh) * 2]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float M_safe = (M == -INFINITY) ? 0.f : M;
+
+  float acc[E], L = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s = 0; s < p.n_split; ++s) {
+    const size_t slot = size_t(s) * p.BH + bh;
+    const float ms = p.part_ml[slot * 2 + 0];
+    const float ls = p.part_ml[slot * 2 + 1];
+    const float w = ex2_approx(ms - M_safe);
+    L = fmaf(ls, w, L);
+    const float* po = p.part_o + slot * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(po[e], w, acc[e]);
+  }
+  const float inv = 1.f / L;
+  __nv_bfloat16* orow = p.o + size_t(bh) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  if (lane == 0 && p.lse != nullptr) p.lse[bh] = (M + __log2f(L)) * kLn2;
+}
+
+template <int D>
+int launch(const DecParams& p, cudaStream_t stream) {
+  const long long nblk = (long long)p.BH * p.n_split;
+  if (nblk > 0x7fffffffLL) return -2;
+  fa_decode_split_kernel<D><<<dim3(unsigned(nblk)), dim3(kDecThreads), 0, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  const int warps_per_blk = 256 / 32;
+  const unsigned cblk = unsigned((p.BH + warps_per_blk - 1) / warps_per_blk);
+  fa_decode_combine_kernel<D><<<dim3(cblk), dim3(256), 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace
+
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int Lk,
+                  int D, float scale, int n_split, float* workspace, cudaStream_t stream) {
+  DecParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = BH;
+  p.Lk = Lk;
+  p.n_split = n_split;
+  p.chunk = (Lk + n_split - 1) / n_split;
+  p.part_o = workspace;
+  p.part_ml = workspace + size_t(n_split) * BH * D;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  if (D == 64) return launch<64>(p, stream);
+  if (D == 128) return launch<128>(p, stream);
+  return -2;
+}
+
+}  // namespace fa

@@ -1,0 +1,38 @@
+// fa_internal.h - host-side launchers shared between the C-ABI translation
+// unit and the kernel translation units (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Wait-site identifiers recorded in the device error word when a bounded wait gives up.
+enum WaitSite : int {
+  kSiteNone = 0,
+  kSiteProducerEmpty = 1,
+  kSiteMmaQ = 2,
+  kSiteMmaK = 3,
+  kSiteMmaV = 4,
+  kSiteMmaP = 5,
+  kSiteSoftmaxS = 6,
+  kSiteSoftmaxO = 7,
+  kSiteSelftest = 8,
+};
+
+// Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err);
+
+// Single-query split-K/V path (Lq == 1).  Arguments already validated.
+// `workspace` must hold n_split * B * H * (D + 2) floats.
+int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
+                  int Lk, int D, float scale, int n_split, float* workspace, cudaStream_t stream);
+
+int num_sms_of_current_device(int* num_sms);
+
+// TMA tensor map over a [BH, L, D] bf16 tensor: box = 64 columns x 128 rows x 1 head,
+// 128-byte swizzle, rows past L read as zeros.  Returns 0 or FA_ERR_CUDA.
+int make_tensor_map_bf16(CUtensorMap* map, const void* ptr, int BH, int L, int D);
+
+}  // namespace fa

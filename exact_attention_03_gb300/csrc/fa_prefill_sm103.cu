@@ -1,0 +1,466 @@
+// fa_prefill_sm103.cu - attention forward for Lq >= 1 on sm_103a.
+//
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
+// streams that head's K/V in 128-key tiles through a shared-memory ring.
+// Both matrix products run on the 5th-generation tensor cores:
+//   S_t = Q_t K_j^T   tcgen05.mma, A = Q_t (smem), B = K_j (smem), fp32 in TMEM
+//   O_t += P_t V_j    tcgen05.mma, A = P_t (TMEM, bf16), B = V_j (smem), fp32 in TMEM
+// and the softmax runs in between on CUDA cores, one thread per query row.
+//
+// The per-row update is the online-softmax recurrence of "NTU Hung-yi Lee ML
+// 2026 Guide: Faster Generation, Part 1: Flash Attention" (quidproquo.cc),
+// "Expand: why multiplying by exp(d1 - d2) fixes it" and "Expand: the
+// correction for the output O": with d the running max and s the running
+// denominator, a new tile moves d to max(d, tile max), multiplies s and O by
+// exp(d_old - d_new) and adds the tile's terms.  The kernel keeps O
+// unnormalised (the guide's O_k multiplied through by s_k) and divides by s
+// once at the end, which is the same quantity.  It works in base 2:
+// x = score * scale * log2(e), exp(a - d) = 2^(x - m).  A rescale is only
+// applied when the running max grows by more than kRescaleLog2 (2^8): for
+// any common reference value the ratio O/s is unchanged (the guide's rescale
+// identity holds for any d2), and bounding the growth keeps 2^(x - m) <= 2^8.
+//
+// Warp roles (12 warps, 384 threads, one CTA per SM):
+//   warp 0        TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... into the ring
+//   warp 1        TMEM allocation; lane 0 issues every tcgen05.mma and commit
+//   warps 2-3     idle (keep the softmax warpgroups aligned to TMEM lane quarters)
+//   warps 4-7     softmax + epilogue for Q0 (TMEM lanes 0-127 = its 128 rows)
+//   warps 8-11    softmax + epilogue for Q1
+// Issue order of the MMA thread (ping-pong between the two query tiles, so the
+// tensor core works on one tile while the other tile's softmax runs):
+//   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
+// P_t (bf16 pairs, 64 columns) overwrites columns [64,128) of S_t after the
+// softmax has read all of S_t into registers.  The next S_t MMA is issued
+// after PV_t, and tcgen05.mma operations from one thread execute in order.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 384;
+// Registers per thread after the role split: 128 threads x kRegsCtl + 256 x
+// kRegsSoftmax = 61440 <= 384 x 168 (the launch allocation).
+constexpr uint32_t kRegsCtl = 64;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kSubBytes = 128 * 128;  // one 128-row x 64-column bf16 sub-block (16 KB)
+
+template <int D>
+struct Cfg {
+  static constexpr int kSub = D / 64;              // 128-byte column blocks per row
+  static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kQOff = 0;
+  static constexpr int kSlotOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kSlotOff + kStages * kTileBytes;
+  // barriers: q_full[2] full[S] empty[S] s_full[2] p_full[2] o_full[2] mma_done
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarFull = 16;
+  static constexpr int kBarEmpty = kBarFull + 8 * kStages;
+  static constexpr int kBarS = kBarEmpty + 8 * kStages;
+  static constexpr int kBarP = kBarS + 16;
+  static constexpr int kBarO = kBarP + 16;
+  static constexpr int kBarDone = kBarO + 16;
+  static constexpr int kTmemHolder = kBarDone + 8;
+  static constexpr int kAbort = kTmemHolder + 4;
+  static constexpr int kMiscBytes = 256;
+  static_assert(kAbort + 4 <= kMiscBytes, "barrier area overflow");
+  static constexpr int kSmemBytes = kBarOff + kMiscBytes + 1024;  // + alignment slack
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int* err;
+  int BH, Lq, Lk;
+  int n_qblk;       // ceil(Lq / 256)
+  int causal;
+  float scale_log2;  // scale * log2(e)
+};
+
+// Bounded wait that ignores the abort flag: used only to drain this CTA's own
+// asynchronous operations before exit.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > 50000000ull) return;  // 50 ms
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base + C::kQOff;
+  const uint32_t sSlot = base + C::kSlotOff;
+  const uint32_t sBar = base + C::kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + C::kTmemHolder);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + C::kAbort);
+
+  auto bar_q = [&](int t) { return sBar + C::kBarQ + 8 * t; };
+  auto bar_full = [&](int s) { return sBar + C::kBarFull + 8 * s; };
+  auto bar_empty = [&](int s) { return sBar + C::kBarEmpty + 8 * s; };
+  auto bar_s = [&](int t) { return sBar + C::kBarS + 8 * t; };
+  auto bar_p = [&](int t) { return sBar + C::kBarP + 8 * t; };
+  auto bar_o = [&](int t) { return sBar + C::kBarO + 8 * t; };
+  const uint32_t bar_done = sBar + C::kBarDone;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which query tiles this CTA owns (heaviest query blocks first)
+  const int qblk = p.n_qblk - 1 - int(blockIdx.x) / p.BH;
+  const int bh = int(blockIdx.x) % p.BH;
+  const int q0 = qblk * 256;
+  const int nk_all = (p.Lk + 127) / 128;
+  int nt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = q0 + 128 * t;
+    if (qt >= p.Lq) {
+      nt[t] = 0;
+    } else if (p.causal) {
+      const int last_row = min(qt + 127, p.Lq - 1);
+      nt[t] = min(nk_all, last_row / 128 + 1);
+    } else {
+      nt[t] = nk_all;
+    }
+  }
+  const int nkv = max(nt[0], nt[1]);
+
+  // ---- setup: barriers, TMEM
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q(0), 1);
+    mbar_init(bar_q(1), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_p(t), 128);
+      mbar_init(bar_o(t), 1);
+    }
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  // warp-uniform warpgroup index (the shuffle makes the uniformity explicit)
+  const int wgrp = __shfl_sync(0xffffffffu, int(threadIdx.x) / 128, 0);
+
+  if (wgrp == 0) {
+    setmaxnreg_dec<kRegsCtl>();
+  if (warp == 0) {
+    // =================== TMA producer ===================
+    if (lane == 0) {
+      int issued = 0;
+      mbar_arrive_expect_tx(bar_q(0), C::kTileBytes);
+#pragma unroll
+      for (int sb = 0; sb < C::kSub; ++sb)
+        tma_load_3d(sQ + sb * kSubBytes, &tmQ, bar_q(0), sb * 64, q0, bh);
+      if (nt[1] > 0) {
+        mbar_arrive_expect_tx(bar_q(1), C::kTileBytes);
+#pragma unroll
+        for (int sb = 0; sb < C::kSub; ++sb)
+          tma_load_3d(sQ + C::kTileBytes + sb * kSubBytes, &tmQ, bar_q(1), sb * 64, q0 + 128, bh);
+      }
+      for (int it = 0; it < 2 * nkv; ++it) {
+        const int s = it % C::kStages;
+        const int use = it / C::kStages;
+        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
+        const uint32_t dst = sSlot + s * C::kTileBytes;
+        const CUtensorMap* map = (it & 1) ? &tmV : &tmK;
+        mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
+#pragma unroll
+        for (int sb = 0; sb < C::kSub; ++sb)
+          tma_load_3d(dst + sb * kSubBytes, map, bar_full(s), sb * 64, (it >> 1) * 128, bh);
+        ++issued;
+      }
+      // drain: every copy this thread started has landed before the CTA exits
+      drain_wait(bar_q(0), 0);
+      if (nt[1] > 0) drain_wait(bar_q(1), 0);
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
+        drain_wait(bar_full(s), (last / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // =================== MMA issuer ===================
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, false, true);
+      // K-major operands (Q, K): 8-row atoms 1024 B apart.  MN-major operand (V):
+      // 8-key groups 1024 B apart, 64-column blocks kSubBytes apart.
+      constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);
+      constexpr uint64_t kDescMN = sdesc_sw128(0, kSubBytes, 1024);
+      bool ok = true;
+      auto wait = [&](uint32_t b, uint32_t ph, int site) {
+        if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
+        return ok;
+      };
+      auto slot = [&](int it) { return it % C::kStages; };
+      auto phase = [&](int it) { return uint32_t((it / C::kStages) & 1); };
+      // S_t = Q_t K_j^T: M = 128 rows, N = 128 keys, K = D in steps of 16
+      auto issue_qk = [&](int t, int j) {
+        const uint32_t a0 = sQ + t * C::kTileBytes;
+        const uint32_t b0 = sSlot + slot(2 * j) * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+          umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + off), sdesc_at(kDescK, b0 + off), kIdQK,
+                  kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t += P_t V_j: M = 128 rows, N = D, K = 128 keys in steps of 16
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t b0 = sSlot + slot(2 * j + 1) * C::kTileBytes;
+        const uint32_t tP = tmem + t * 128 + 64;
+        const uint32_t tO = tmem + 256 + t * D;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          umma_ts(tO, tP + kk * 8, sdesc_at(kDescMN, b0 + kk * 16 * 128), kIdPV,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      wait(bar_q(0), 0, kSiteMmaQ);
+      if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
+      if (wait(bar_full(slot(0)), phase(0), kSiteMmaK)) {
+        tc_fence_after();
+        if (nt[0] > 0) {
+          issue_qk(0, 0);
+          umma_commit(bar_s(0));
+        }
+        if (nt[1] > 0) {
+          issue_qk(1, 0);
+          umma_commit(bar_s(1));
+        }
+        umma_commit(bar_empty(slot(0)));
+      }
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!wait(bar_full(slot(2 * j + 1)), phase(2 * j + 1), kSiteMmaV)) break;
+        tc_fence_after();
+        if (j < nt[0]) {
+          if (!wait(bar_p(0), j & 1, kSiteMmaP)) break;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j == nt[0] - 1) umma_commit(bar_o(0));
+        }
+        const bool next_k = (j + 1 < nkv);
+        if (next_k) {
+          if (!wait(bar_full(slot(2 * j + 2)), phase(2 * j + 2), kSiteMmaK)) break;
+          tc_fence_after();
+        }
+        if (j + 1 < nt[0]) {
+          issue_qk(0, j + 1);
+          umma_commit(bar_s(0));
+        }
+        if (j < nt[1]) {
+          if (!wait(bar_p(1), j & 1, kSiteMmaP)) break;
+          tc_fence_after();
+          issue_pv(1, j);
+          if (j == nt[1] - 1) umma_commit(bar_o(1));
+        }
+        umma_commit(bar_empty(slot(2 * j + 1)));
+        if (j + 1 < nt[1]) {
+          issue_qk(1, j + 1);
+          umma_commit(bar_s(1));
+        }
+        if (next_k) umma_commit(bar_empty(slot(2 * j + 2)));
+      }
+      // every MMA issued above has completed before TMEM is released
+      umma_commit(bar_done);
+      drain_wait(bar_done, 0);
+    }
+  }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
+    // =================== softmax + epilogue ===================
+    const int t = (warp - 4) >> 2;
+    const int g = warp & 3;                      // TMEM lane quarter of this warp
+    const int r = g * 32 + lane;                 // row within the query tile
+    const int qt = q0 + 128 * t;
+    const int qrow = qt + r;
+    const uint32_t lane_off = uint32_t(g * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tP = tS + 64;
+    const uint32_t tO = tmem + lane_off + 256 + t * D;
+    const float c = p.scale_log2;
+    float m_run = -INFINITY;  // running max, log2 units
+    float l_run = 0.f;        // running denominator relative to m_run
+    bool ok = true;
+    const int n = t ? nt[1] : nt[0];
+
+    for (int j = 0; j < n; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+      tmem_ld128_sync(tS, s);
+
+      const int k0 = j * 128;
+      const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
+      if (edge) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          const int key = k0 + i;
+          if (key >= p.Lk || (p.causal && key > qrow)) s[i] = -INFINITY;
+        }
+      }
+      float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+      for (int i = 2; i < 128; i += 2) {
+        mx0 = fmaxf(mx0, s[i]);
+        mx1 = fmaxf(mx1, s[i + 1]);
+      }
+      const float m_cand = fmaxf(m_run, fmaxf(mx0, mx1) * c);
+      const bool need = (m_cand - m_run) > kRescaleLog2;  // true on the first tile
+      const bool any = __any_sync(0xffffffffu, need);
+      const float m_use = any ? m_cand : m_run;
+      const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
+      const float alpha = ex2_approx(m_run - m_safe);    // 0 on the first tile
+      m_run = m_use;
+
+      // P = 2^(x - m) in bf16 pairs, written over columns [64,128) of S
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(s[32 * cb + 2 * i], c, -m_safe));
+          const float p1 = ex2_approx(fmaf(s[32 * cb + 2 * i + 1], c, -m_safe));
+          rs0 += p0;
+          rs1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tP + 16 * cb, pk);
+      }
+      l_run = l_run * alpha + (rs0 + rs1);
+
+      // rescale O: PV of tile j-1 has completed (S_t(j)'s commit was issued after it)
+      if (any && j > 0) {
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          float ov[32];
+          tmem_ld32_sync(tO + cc, ov);
+          uint32_t w[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(ov[i] * alpha);
+          tmem_st32(tO + cc, w);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar_p(t));
+    }
+
+    // epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), 0, abort_flag, p.err, kSiteSoftmaxO));
+    if (ok && n > 0) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      const bool valid = qrow < p.Lq;
+      __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        float ov[32];
+        tmem_ld32_sync(tO + cc, ov);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+      if (valid && p.lse != nullptr) p.lse[size_t(bh) * p.Lq + qrow] = (m_run + __log2f(l_run)) * kLn2;
+    }
+  }
+
+  // ---- teardown: all TMEM traffic of this CTA is finished
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
+           int Lk, float scale, int causal, cudaStream_t stream, int* err);
+
+}  // namespace
+
+namespace {
+template <int D>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
+           int Lk, float scale, int causal, cudaStream_t stream, int* err) {
+  using C = Cfg<D>;
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  int st = make_tensor_map_bf16(&mq, q, BH, Lq, D);
+  if (st == 0) st = make_tensor_map_bf16(&mk, k, BH, Lk, D);
+  if (st == 0) st = make_tensor_map_bf16(&mv, v, BH, Lk, D);
+  if (st != 0) return st;
+
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = err;
+  p.BH = BH;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.n_qblk = (Lq + 255) / 256;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+
+  static_assert(C::kSmemBytes <= 232448, "shared memory budget");
+  if (cudaFuncSetAttribute(fa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return -4;
+  const long long nblk = (long long)p.n_qblk * BH;
+  if (nblk > 0x7fffffffLL) return -2;
+  fa_prefill_kernel<D><<<dim3(unsigned(nblk)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+}  // namespace
+
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err) {
+  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
+  if (D == 128) return launch<128>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
+  return -2;
+}
+
+}  // namespace fa

@@ -1,0 +1,118 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention forward library.
+ *
+ * The library computes exact scaled-dot-product attention
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,   LSE = ln sum_j exp(scale * q.k_j)
+ *
+ * in one pass over K/V tiles, with the online-softmax recurrence derived in
+ * "NTU Hung-yi Lee ML 2026 Guide: Faster Generation, Part 1: Flash Attention"
+ * (quidproquo.cc), sections "Mechanism: run with the wrong answer, then
+ * correct it", "Expand: why multiplying by exp(d1 - d2) fixes it" and
+ * "Expand: the correction for the output O": a running maximum d, a running
+ * denominator s rescaled by exp(d_old - d_new), and a running output rescaled
+ * the same way, so that the attention weights are never written to memory
+ * ("Back to real models": no attention weights are returned).  The per-row
+ * statistics m (max) and l (sum) are those of "6.3 FlashAttention"
+ * (comfyai.app), "How FlashAttention Works"; LSE = m + ln l is exported as
+ * their natural-log summary.
+ *
+ * Every entry point is a plain C function: pointers, sizes and a status
+ * code.  No entry point takes or returns a PyTorch or C++ type.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (returned by every entry point). */
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, non-finite or non-positive scale */
+  FA_ERR_UNSUPPORTED = -2,  /* valid but not implemented: head dim not in {64,128}, causal with Lq != Lk, size limits */
+  FA_ERR_MISALIGNED = -3,   /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+  FA_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed (no device, launch failure, ...) */
+  FA_ERR_TIMEOUT = -5       /* a device-side wait gave up (reported by fa_last_device_error) */
+} fa_status;
+
+/*
+ * fa_fwd - attention forward pass on the GPU.
+ *
+ * q     : device pointer, bf16, [B, H, Lq, D], contiguous (row-major, D fastest).
+ * k, v  : device pointers, bf16, [B, H, Lk, D], contiguous.
+ * o     : device pointer, bf16, [B, H, Lq, D], contiguous; written.
+ * lse   : device pointer, fp32, [B, H, Lq]; written with the natural-log
+ *         log-sum-exp of the scaled scores of each query row; may be NULL.
+ * B, H  : batch size and number of heads (each head attends independently).
+ * Lq, Lk: number of query and key/value positions (>= 1).
+ * D     : head dimension, 64 or 128.
+ * scale : score scale (typically 1/sqrt(D)); finite and > 0.
+ * causal: 0 = every key visible; 1 = key j visible to query i iff j <= i
+ *         (requires Lq == Lk).
+ * stream: the cudaStream_t to enqueue on (NULL = legacy default stream).
+ *
+ * Ownership: the caller owns every buffer; the library keeps no pointer after
+ * the call returns.  The single-query path (Lq == 1, non-causal) splits the
+ * keys over many thread blocks and needs a workspace of
+ * n_split * B * H * (D + 2) * 4 bytes, which it allocates and frees
+ * stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ *
+ * Errors: arguments are checked on the host before any CUDA call, and a bad
+ * argument returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_MISALIGNED
+ * without touching the GPU.  A failing CUDA call returns FA_ERR_CUDA.
+ * Like any kernel launch the call is asynchronous: FA_OK means "enqueued".
+ * Device-side waits are bounded; one that gives up records FA_ERR_TIMEOUT,
+ * readable with fa_last_device_error.  q/k/v must not alias o or lse.
+ * Thread safety: reentrant; calls on different streams may overlap.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int Lq, int Lk, int D, float scale, int causal,
+           void* stream);
+
+/*
+ * fa_strerror - static, NUL-terminated description of a status code.
+ * Never returns NULL; unknown codes give "unknown fa_status".
+ */
+const char* fa_strerror(int status);
+
+/*
+ * fa_last_device_error - synchronises `stream`, then reads and clears the
+ * library's device error word on the current device.  Returns FA_OK when no
+ * device-side wait has given up since the last call, else FA_ERR_TIMEOUT
+ * (FA_ERR_CUDA if the synchronisation itself fails).  If `site` is not NULL it
+ * receives an identifier of the wait that gave up (0 when none).
+ */
+int fa_last_device_error(void* stream, int* site);
+
+/*
+ * fa_decode_num_splits - the number of key splits the single-query path uses
+ * for a problem of B*H heads with Lk keys on a GPU with `num_sms` SMs
+ * (host-only arithmetic; no CUDA call).  Returns >= 1, or FA_ERR_INVALID_ARG.
+ */
+int fa_decode_num_splits(int BH, int Lk, int num_sms);
+
+/*
+ * fa_wait_selftest - launches one block whose single thread waits on a
+ * shared-memory barrier that nothing ever completes, with a wait limit of
+ * `limit_us` microseconds (1..10,000,000).  The wait must give up, record
+ * FA_ERR_TIMEOUT in the device error word and return.  The call synchronises
+ * `stream` and returns what fa_last_device_error then reads (FA_ERR_TIMEOUT
+ * when the bounded wait works).  It exercises the same bounded-wait routine
+ * the attention kernels use, without faulting or hanging the GPU.
+ */
+int fa_wait_selftest(int limit_us, void* stream);
+
+/* fa_abi_version - (major << 16) | minor of this header's ABI. */
+int fa_abi_version(void);
+
+#define FA_ABI_VERSION ((1 << 16) | 0)
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,135 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+include/fa.h declares, and rejects bad arguments before any CUDA call.
+No kernel is launched here (bad arguments never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_03_gb300 as fa
+from exact_attention_03_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_expected_entry_points():
+    names = declared_functions()
+    for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
+              "fa_wait_selftest", "fa_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    # and the binding knows the signature of each of them
+    assert set(declared_functions()) <= set(fa.EXPORTED_SYMBOLS)
+
+
+def test_abi_version(lib):
+    assert lib.fa_abi_version() == (1 << 16)
+
+
+def test_strerror_covers_every_status(lib):
+    for code in range(0, -6, -1):
+        s = fa.strerror(code)
+        assert s and "unknown" not in s
+    assert "unknown" in fa.strerror(-99)
+
+
+A = 0x10000  # a 16-byte aligned fake address; calls below never dereference it
+
+
+def call(**kw):
+    args = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Lq=128, Lk=128, D=128, scale=0.1, causal=0)
+    args.update(kw)
+    return fa.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["lse"], args["B"], args["H"],
+                     args["Lq"], args["Lk"], args["D"], args["scale"], args["causal"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=None), fa.FA_ERR_INVALID_ARG),
+    (dict(v=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Lq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Lk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(D=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(D=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=1, Lq=64, Lk=128), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(k=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(v=A + 4), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 1), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_bad_arguments_rejected_on_host(lib, kw, expect):
+    assert call(**kw) == expect
+
+
+def test_valid_arguments_without_a_gpu_report_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (the fake pointers must never reach a kernel)")
+    assert call() == fa.FA_ERR_CUDA
+    assert call(Lq=1, Lk=1000) == fa.FA_ERR_CUDA
+    st, site = fa.last_device_error(None)
+    assert st == fa.FA_ERR_CUDA and site == 0
+
+
+@pytest.mark.parametrize("BH,Lk,sms", [(512, 131072, 152), (1, 131072, 152), (32, 256, 148),
+                                       (1, 1, 152), (7, 65, 152), (4096, 100000, 152),
+                                       (1, 10 ** 9, 152), (3, 4097, 1)])
+def test_decode_split_count(lib, BH, Lk, sms):
+    n = fa.decode_num_splits(BH, Lk, sms)
+    assert 1 <= n <= 4096
+    chunk = -(-Lk // n)
+    assert (n - 1) * chunk < Lk, "no split may be empty"
+    assert chunk >= min(64, Lk) or n == 1
+    if (BH, Lk, sms) == (512, 131072, 152):
+        assert n == 64  # 2048 keys per split
+    assert fa.decode_num_splits(0, 10, 10) == fa.FA_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(fa, "_lib", None)
+    monkeypatch.setattr(fa, "_HERE", str(tmp_path))
+    with pytest.raises(ImportError):
+        fa.load()
+
+
+def test_wait_selftest_rejects_bad_limit(lib):
+    assert fa.wait_selftest(0) == fa.FA_ERR_INVALID_ARG
+    assert fa.wait_selftest(10 ** 8) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_rejects_bad_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)  # CPU tensors are refused; no silent fallback
+    with pytest.raises(ValueError):
+        fa.forward(q[0], q, q)
