@@ -314,6 +314,29 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile_case(args):
+    """Runs one workload `reps` times with no flush or timing: the command
+    the ncu captures profile."""
+    import torch
+    import exact_attention_03_gb300 as fa
+    from exact_attention_03_gb300 import build as fa_build
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+
+    fa_build.build()
+    fa.load()
+    w = WORKLOADS[args.profile_case]
+    if args.profile_batch:
+        w = w.with_(B=args.profile_batch)
+    q, k, v = make_inputs(w, "cuda")
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        fa.forward(q, k, v, causal=w.causal)
+    st, site = fa.last_device_error()
+    print(json.dumps({"profile_case": w.name, "B": w.B, "reps": args.reps, "status": st}))
+    if st != fa.FA_OK:
+        sys.exit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -323,7 +346,13 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config section")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--profile-case", default=None, help="run one workload (for ncu captures)")
+    ap.add_argument("--profile-batch", type=int, default=0, help="batch override for --profile-case")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 
