@@ -65,7 +65,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -259,34 +259,42 @@ def per_config(args, fa, flush, dev, peaks, check):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(max_seconds, per_len_rows=None):
-    """Runs the oracle on a bounded sample of the sweep; returns (flops, seconds, desc)."""
+def _oracle_sample(max_seconds, per_len_rows=None, max_rounds=None):
+    """Runs the oracle on a bounded sample of the sweep: round r computes head r
+    (b = r // H, h = r % H) at every length, until `max_seconds` of oracle time
+    or `max_rounds` rounds.  Returns (flops, seconds, description)."""
     import numpy as np
     from exact_attention_03_gb300.inputs import make_inputs
     from oracle.naive import attention_head, to_f64
 
+    ws = sweep_workloads()
+    inputs = [make_inputs(w, "cpu") for w in ws]
     flops = 0.0
     spent = 0.0
-    parts = []
-    for w in sweep_workloads():
-        q, k, v = make_inputs(w.with_(B=1), "cpu")
-        qh, kh, vh = to_f64(q[0, 0]), to_f64(k[0, 0]), to_f64(v[0, 0])
-        rows = w.Lq if per_len_rows is None else min(w.Lq, per_len_rows)
-        t0 = time.perf_counter()
-        attention_head(qh, kh, vh, w.scale, causal=w.causal, rows=np.arange(rows))
-        spent += time.perf_counter() - t0
-        flops += 4.0 * rows * w.Lk * w.D
-        parts.append(f"L={w.Lq}:{rows} rows")
-        if spent > max_seconds:
+    rounds = 0
+    nheads = ws[0].B * ws[0].H
+    while rounds < nheads:
+        b, h = divmod(rounds, ws[0].H)
+        for w, (q, k, v) in zip(ws, inputs):
+            qh, kh, vh = to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h])
+            rows = w.Lq if per_len_rows is None else min(w.Lq, per_len_rows)
+            t0 = time.perf_counter()
+            attention_head(qh, kh, vh, w.scale, causal=w.causal, rows=np.arange(rows))
+            spent += time.perf_counter() - t0
+            flops += 4.0 * rows * w.Lk * w.D
+        rounds += 1
+        if spent > max_seconds or (max_rounds is not None and rounds >= max_rounds):
             break
-    return flops, spent, "head (b=0,h=0) of each sweep length, " + ", ".join(parts)
+    rows_desc = "all rows" if per_len_rows is None else f"first {per_len_rows} rows"
+    return flops, spent, (f"{rounds} head(s) at every sweep length L=64..8192, {rows_desc}"
+                          " per head (numpy fp64, BLAS threads = all host cores)")
 
 
 def cpu_baseline(seconds):
     flops, spent, desc = _oracle_sample(seconds)
     return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOPS",
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": desc + " (numpy fp64, BLAS threads = all host cores)",
+            "sample": desc,
             "seconds": round(spent, 2)}
 
 
@@ -295,7 +303,7 @@ def run_reference(args, rank, world):
         return None
     step = []
     for i in range(args.warmup + args.steps):
-        flops, spent, desc = _oracle_sample(1e9, per_len_rows=128)
+        flops, spent, desc = _oracle_sample(1e9, per_len_rows=256, max_rounds=1)
         if i >= args.warmup:
             step.append((flops, spent))
     flops = sum(f for f, _ in step)
@@ -340,7 +348,7 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config section")

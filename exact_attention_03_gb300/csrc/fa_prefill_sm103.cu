@@ -326,19 +326,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int k0 = j * 128;
       const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
       if (edge) {
+        // keys k0 + i with i < lim are visible: i < Lk - k0, and i <= qrow - k0 when causal
+        const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const int key = k0 + i;
-          if (key >= p.Lk || (p.causal && key > qrow)) s[i] = -INFINITY;
-        }
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) s[i] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1];
+      // row max: 16 independent partial maxima (3-input max), then a short tree
+      float pm[16];
 #pragma unroll
-      for (int i = 2; i < 128; i += 2) {
-        mx0 = fmaxf(mx0, s[i]);
-        mx1 = fmaxf(mx1, s[i + 1]);
+      for (int g2 = 0; g2 < 16; ++g2) {
+        float a = fmax3(s[8 * g2], s[8 * g2 + 1], s[8 * g2 + 2]);
+        a = fmax3(a, s[8 * g2 + 3], s[8 * g2 + 4]);
+        a = fmax3(a, s[8 * g2 + 5], s[8 * g2 + 6]);
+        pm[g2] = fmaxf(a, s[8 * g2 + 7]);
       }
-      const float m_cand = fmaxf(m_run, fmaxf(mx0, mx1) * c);
+      const float mx = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                                   fmax3(pm[6], pm[7], pm[8])),
+                             fmax3(pm[9], pm[10], pm[11]),
+                             fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+      const float m_cand = fmaxf(m_run, mx * c);
       const bool need = (m_cand - m_run) > kRescaleLog2;  // true on the first tile
       const bool any = __any_sync(0xffffffffu, need);
       const float m_use = any ? m_cand : m_run;
@@ -346,22 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = ex2_approx(m_run - m_safe);    // 0 on the first tile
       m_run = m_use;
 
-      // P = 2^(x - m) in bf16 pairs, written over columns [64,128) of S
-      float rs0 = 0.f, rs1 = 0.f;
+      // P = 2^(x - m) in bf16 pairs, written over columns [64,128) of S;
+      // x - m = s * c - m as packed fp32x2 FMAs, row sum in 8 independent chains
+      const float2 c2 = make_float2(c, c);
+      const float2 nm2 = make_float2(-m_safe, -m_safe);
+      float2 acc[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(s[32 * cb + 2 * i], c, -m_safe));
-          const float p1 = ex2_approx(fmaf(s[32 * cb + 2 * i + 1], c, -m_safe));
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 x = __ffma2_rn(make_float2(s[32 * cb + 2 * i], s[32 * cb + 2 * i + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          pk[i] = pack_bf16x2(pr.x, pr.y);
         }
         tmem_st16(tP + 16 * cb, pk);
       }
-      l_run = l_run * alpha + (rs0 + rs1);
+      const float2 a01 = __fadd2_rn(acc[0], acc[1]);
+      const float2 a23 = __fadd2_rn(acc[2], acc[3]);
+      const float2 a03 = __fadd2_rn(a01, a23);
+      l_run = l_run * alpha + (a03.x + a03.y);
 
       // rescale O: PV of tile j-1 has completed (S_t(j)'s commit was issued after it)
       if (any && j > 0) {
