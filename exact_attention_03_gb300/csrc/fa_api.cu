@@ -70,11 +70,14 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
 int make_tensor_map_bf16(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return FA_ERR_CUDA;
-  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(L), cuuint64_t(BH)};
-  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(L) * cuuint64_t(D) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+  // [BH, L, D] seen as {64 columns, L rows, D/64 column blocks, BH heads}: a box
+  // {64, 128, D/64, 1} is one 128-row tile, stored in shared memory as D/64
+  // blocks of 128 rows x 128 bytes (the 128-byte swizzle works per block).
+  const cuuint64_t dims[4] = {64, cuuint64_t(L), cuuint64_t(D / 64), cuuint64_t(BH)};
+  const cuuint64_t strides[3] = {cuuint64_t(D) * 2, 128, cuuint64_t(L) * cuuint64_t(D) * 2};
+  const cuuint32_t box[4] = {64, 128, cuuint32_t(D / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -31,8 +31,9 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
 
 int num_sms_of_current_device(int* num_sms);
 
-// TMA tensor map over a [BH, L, D] bf16 tensor: box = 64 columns x 128 rows x 1 head,
-// 128-byte swizzle, rows past L read as zeros.  Returns 0 or FA_ERR_CUDA.
+// TMA tensor map over a [BH, L, D] bf16 tensor, viewed as {64, L, D/64, BH}: one
+// box is a 128-row tile of one head (D/64 swizzled blocks of 128 rows x 128 B),
+// rows past L read as zeros.  Returns 0 or FA_ERR_CUDA.
 int make_tensor_map_bf16(CUtensorMap* map, const void* ptr, int BH, int L, int D);
 
 }  // namespace fa

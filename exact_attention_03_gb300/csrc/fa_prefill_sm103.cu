@@ -21,9 +21,10 @@
 // identity holds for any d2), and bounding the growth keeps 2^(x - m) <= 2^8.
 //
 // Warp roles (12 warps, 384 threads, one CTA per SM):
-//   warp 0        TMA producer: Q0, Q1 once; then K_0, V_0, K_1, V_1, ... into the ring
+//   warp 0        TMA producer: Q0, Q1 once; then K_0, K_1, ... into the K ring
 //   warp 1        TMEM allocation; lane 0 issues every tcgen05.mma and commit
-//   warps 2-3     idle (keep the softmax warpgroups aligned to TMEM lane quarters)
+//   warp 2        TMA producer: V_0, V_1, ... into the V ring
+//   warp 3        idle (keeps the softmax warpgroups aligned to TMEM lane quarters)
 //   warps 4-7     softmax + epilogue for Q0 (TMEM lanes 0-127 = its 128 rows)
 //   warps 8-11    softmax + epilogue for Q1
 // Issue order of the MMA thread (ping-pong between the two query tiles, so the
@@ -53,16 +54,20 @@ constexpr int kSubBytes = 128 * 128;  // one 128-row x 64-column bf16 sub-block 
 template <int D>
 struct Cfg {
   static constexpr int kSub = D / 64;              // 128-byte column blocks per row
-  static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile (one TMA box)
+  static constexpr int kKStages = (D == 128) ? 2 : 4;   // K ring
+  static constexpr int kVStages = (D == 128) ? 2 : 4;   // V ring
   static constexpr int kQOff = 0;
-  static constexpr int kSlotOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kSlotOff + kStages * kTileBytes;
-  // barriers: q_full[2] full[S] empty[S] s_full[2] p_full[2] o_full[2] mma_done
+  static constexpr int kKOff = 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  // barriers: q_full[2] kfull[SK] kempty[SK] vfull[SV] vempty[SV] s_full[2] p_full[2] o_full[2] mma_done
   static constexpr int kBarQ = 0;
-  static constexpr int kBarFull = 16;
-  static constexpr int kBarEmpty = kBarFull + 8 * kStages;
-  static constexpr int kBarS = kBarEmpty + 8 * kStages;
+  static constexpr int kBarKFull = 16;
+  static constexpr int kBarKEmpty = kBarKFull + 8 * kKStages;
+  static constexpr int kBarVFull = kBarKEmpty + 8 * kKStages;
+  static constexpr int kBarVEmpty = kBarVFull + 8 * kVStages;
+  static constexpr int kBarS = kBarVEmpty + 8 * kVStages;
   static constexpr int kBarP = kBarS + 16;
   static constexpr int kBarO = kBarP + 16;
   static constexpr int kBarDone = kBarO + 16;
@@ -104,14 +109,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
 
   const uint32_t sQ = base + C::kQOff;
-  const uint32_t sSlot = base + C::kSlotOff;
+  const uint32_t sK = base + C::kKOff;
+  const uint32_t sV = base + C::kVOff;
   const uint32_t sBar = base + C::kBarOff;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + C::kTmemHolder);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + C::kAbort);
 
   auto bar_q = [&](int t) { return sBar + C::kBarQ + 8 * t; };
-  auto bar_full = [&](int s) { return sBar + C::kBarFull + 8 * s; };
-  auto bar_empty = [&](int s) { return sBar + C::kBarEmpty + 8 * s; };
+  auto bar_kfull = [&](int s) { return sBar + C::kBarKFull + 8 * s; };
+  auto bar_kempty = [&](int s) { return sBar + C::kBarKEmpty + 8 * s; };
+  auto bar_vfull = [&](int s) { return sBar + C::kBarVFull + 8 * s; };
+  auto bar_vempty = [&](int s) { return sBar + C::kBarVEmpty + 8 * s; };
   auto bar_s = [&](int t) { return sBar + C::kBarS + 8 * t; };
   auto bar_p = [&](int t) { return sBar + C::kBarP + 8 * t; };
   auto bar_o = [&](int t) { return sBar + C::kBarO + 8 * t; };
@@ -144,9 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q(0), 1);
     mbar_init(bar_q(1), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(bar_kfull(s), 1);
+      mbar_init(bar_kempty(s), 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(bar_vfull(s), 1);
+      mbar_init(bar_vempty(s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
@@ -175,38 +187,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (wgrp == 0) {
     setmaxnreg_dec<kRegsCtl>();
-  if (warp == 0) {
-    // =================== TMA producer ===================
+  if (warp == 0 || warp == 2) {
+    // =================== TMA producers ===================
+    // Warp 0 streams Q and K, warp 2 streams V: TMA boxes issued by one thread
+    // are processed one after the other, so two issuing threads double the
+    // load rate.  One box = one 128-row tile (all D columns, D/64 swizzled
+    // 128-byte column blocks).
     if (lane == 0) {
-      int issued = 0;
-      mbar_arrive_expect_tx(bar_q(0), C::kTileBytes);
-#pragma unroll
-      for (int sb = 0; sb < C::kSub; ++sb)
-        tma_load_3d(sQ + sb * kSubBytes, &tmQ, bar_q(0), sb * 64, q0, bh);
-      if (nt[1] > 0) {
-        mbar_arrive_expect_tx(bar_q(1), C::kTileBytes);
-#pragma unroll
-        for (int sb = 0; sb < C::kSub; ++sb)
-          tma_load_3d(sQ + C::kTileBytes + sb * kSubBytes, &tmQ, bar_q(1), sb * 64, q0 + 128, bh);
+      const bool is_k = (warp == 0);
+      const int NS = is_k ? C::kKStages : C::kVStages;
+      const uint32_t ring = is_k ? sK : sV;
+      const CUtensorMap* map = is_k ? &tmK : &tmV;
+      if (is_k) {
+        mbar_arrive_expect_tx(bar_q(0), C::kTileBytes);
+        tma_load_tile(sQ, &tmQ, bar_q(0), q0, bh);
+        if (nt[1] > 0) {
+          mbar_arrive_expect_tx(bar_q(1), C::kTileBytes);
+          tma_load_tile(sQ + C::kTileBytes, &tmQ, bar_q(1), q0 + 128, bh);
+        }
       }
-      for (int it = 0; it < 2 * nkv; ++it) {
-        const int s = it % C::kStages;
-        const int use = it / C::kStages;
-        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
-        const uint32_t dst = sSlot + s * C::kTileBytes;
-        const CUtensorMap* map = (it & 1) ? &tmV : &tmK;
-        mbar_arrive_expect_tx(bar_full(s), C::kTileBytes);
-#pragma unroll
-        for (int sb = 0; sb < C::kSub; ++sb)
-          tma_load_3d(dst + sb * kSubBytes, map, bar_full(s), sb * 64, (it >> 1) * 128, bh);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % NS;
+        const int use = j / NS;
+        const uint32_t empty = is_k ? bar_kempty(s) : bar_vempty(s);
+        const uint32_t full = is_k ? bar_kfull(s) : bar_vfull(s);
+        if (!mbar_wait(empty, (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        tma_load_tile(ring + s * C::kTileBytes, map, full, j * 128, bh);
         ++issued;
       }
       // drain: every copy this thread started has landed before the CTA exits
-      drain_wait(bar_q(0), 0);
-      if (nt[1] > 0) drain_wait(bar_q(1), 0);
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
-        drain_wait(bar_full(s), (last / C::kStages) & 1);
+      if (is_k) {
+        drain_wait(bar_q(0), 0);
+        if (nt[1] > 0) drain_wait(bar_q(1), 0);
+      }
+      for (int s = 0; s < NS && s < issued; ++s) {
+        const int last = s + NS * ((issued - 1 - s) / NS);
+        drain_wait(is_k ? bar_kfull(s) : bar_vfull(s), (last / NS) & 1);
       }
     }
   } else if (warp == 1) {
@@ -223,12 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
         return ok;
       };
-      auto slot = [&](int it) { return it % C::kStages; };
-      auto phase = [&](int it) { return uint32_t((it / C::kStages) & 1); };
+      auto kslot = [&](int j) { return j % C::kKStages; };
+      auto kphase = [&](int j) { return uint32_t((j / C::kKStages) & 1); };
+      auto vslot = [&](int j) { return j % C::kVStages; };
+      auto vphase = [&](int j) { return uint32_t((j / C::kVStages) & 1); };
       // S_t = Q_t K_j^T: M = 128 rows, N = 128 keys, K = D in steps of 16
       auto issue_qk = [&](int t, int j) {
         const uint32_t a0 = sQ + t * C::kTileBytes;
-        const uint32_t b0 = sSlot + slot(2 * j) * C::kTileBytes;
+        const uint32_t b0 = sK + kslot(j) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
@@ -238,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // O_t += P_t V_j: M = 128 rows, N = D, K = 128 keys in steps of 16
       auto issue_pv = [&](int t, int j) {
-        const uint32_t b0 = sSlot + slot(2 * j + 1) * C::kTileBytes;
+        const uint32_t b0 = sV + vslot(j) * C::kTileBytes;
         const uint32_t tP = tmem + t * 128 + 64;
         const uint32_t tO = tmem + 256 + t * D;
 #pragma unroll
@@ -250,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       wait(bar_q(0), 0, kSiteMmaQ);
       if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
-      if (wait(bar_full(slot(0)), phase(0), kSiteMmaK)) {
+      if (wait(bar_kfull(kslot(0)), kphase(0), kSiteMmaK)) {
         tc_fence_after();
         if (nt[0] > 0) {
           issue_qk(0, 0);
@@ -260,10 +280,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_qk(1, 0);
           umma_commit(bar_s(1));
         }
-        umma_commit(bar_empty(slot(0)));
+        umma_commit(bar_kempty(kslot(0)));
       }
       for (int j = 0; j < nkv && ok; ++j) {
-        if (!wait(bar_full(slot(2 * j + 1)), phase(2 * j + 1), kSiteMmaV)) break;
+        if (!wait(bar_vfull(vslot(j)), vphase(j), kSiteMmaV)) break;
         tc_fence_after();
         if (j < nt[0]) {
           if (!wait(bar_p(0), j & 1, kSiteMmaP)) break;
@@ -273,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool next_k = (j + 1 < nkv);
         if (next_k) {
-          if (!wait(bar_full(slot(2 * j + 2)), phase(2 * j + 2), kSiteMmaK)) break;
+          if (!wait(bar_kfull(kslot(j + 1)), kphase(j + 1), kSiteMmaK)) break;
           tc_fence_after();
         }
         if (j + 1 < nt[0]) {
@@ -286,12 +306,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(1, j);
           if (j == nt[1] - 1) umma_commit(bar_o(1));
         }
-        umma_commit(bar_empty(slot(2 * j + 1)));
+        umma_commit(bar_vempty(vslot(j)));
         if (j + 1 < nt[1]) {
           issue_qk(1, j + 1);
           umma_commit(bar_s(1));
         }
-        if (next_k) umma_commit(bar_empty(slot(2 * j + 2)));
+        if (next_k) umma_commit(bar_kempty(kslot(j + 1)));
       }
       // every MMA issued above has completed before TMEM is released
       umma_commit(bar_done);
