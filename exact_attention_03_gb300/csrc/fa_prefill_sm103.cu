@@ -44,8 +44,8 @@ namespace {
 
 constexpr int kThreads = 384;
 // Registers per thread after the role split: 128 threads x kRegsCtl + 256 x
-// kRegsSoftmax = 61440 <= 384 x 168 (the launch allocation).
-constexpr uint32_t kRegsCtl = 64;
+// kRegsSoftmax = 63488 <= 384 x 168 (the launch allocation).
+constexpr uint32_t kRegsCtl = 80;
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
@@ -241,77 +241,93 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
         return ok;
       };
-      auto kslot = [&](int j) { return j % C::kKStages; };
-      auto kphase = [&](int j) { return uint32_t((j / C::kKStages) & 1); };
-      auto vslot = [&](int j) { return j % C::kVStages; };
-      auto vphase = [&](int j) { return uint32_t((j / C::kVStages) & 1); };
-      // S_t = Q_t K_j^T: M = 128 rows, N = 128 keys, K = D in steps of 16
-      auto issue_qk = [&](int t, int j) {
+      // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16
+      auto issue_qk = [&](int t, uint32_t kaddr) {
         const uint32_t a0 = sQ + t * C::kTileBytes;
-        const uint32_t b0 = sK + kslot(j) * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + off), sdesc_at(kDescK, b0 + off), kIdQK,
+          umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + off), sdesc_at(kDescK, kaddr + off), kIdQK,
                   kk > 0 ? 1u : 0u);
         }
       };
-      // O_t += P_t V_j: M = 128 rows, N = D, K = 128 keys in steps of 16
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t b0 = sV + vslot(j) * C::kTileBytes;
+      // O_t += P_t V: M = 128 rows, N = D, K = 128 keys in steps of 16
+      auto issue_pv = [&](int t, uint32_t vaddr, bool accumulate) {
         const uint32_t tP = tmem + t * 128 + 64;
         const uint32_t tO = tmem + 256 + t * D;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          umma_ts(tO, tP + kk * 8, sdesc_at(kDescMN, b0 + kk * 16 * 128), kIdPV,
-                  (j > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tO, tP + kk * 8, sdesc_at(kDescMN, vaddr + kk * 16 * 128), kIdPV,
+                  (accumulate || kk > 0) ? 1u : 0u);
         }
       };
 
+      // A wait stalls this thread for several hundred cycles, and the tensor
+      // core idles unless that much MMA work is already queued: every wait
+      // below sits between two MMA groups, never two waits in a row.
+      // Ring positions (slot, phase) of K_j and V_j advance incrementally.
+      int ks = 0, vs = 0;
+      uint32_t kph = 0, vph = 0;
       wait(bar_q(0), 0, kSiteMmaQ);
       if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
-      if (wait(bar_kfull(kslot(0)), kphase(0), kSiteMmaK)) {
+      if (wait(bar_kfull(0), 0, kSiteMmaK)) {
         tc_fence_after();
         if (nt[0] > 0) {
-          issue_qk(0, 0);
+          issue_qk(0, sK);
           umma_commit(bar_s(0));
         }
         if (nt[1] > 0) {
-          issue_qk(1, 0);
+          issue_qk(1, sK);
           umma_commit(bar_s(1));
         }
-        umma_commit(bar_kempty(kslot(0)));
+        umma_commit(bar_kempty(0));
       }
+      wait(bar_vfull(0), 0, kSiteMmaV);
       for (int j = 0; j < nkv && ok; ++j) {
-        if (!wait(bar_vfull(vslot(j)), vphase(j), kSiteMmaV)) break;
-        tc_fence_after();
+        const uint32_t vaddr = sV + vs * C::kTileBytes;
+        const int ks1 = (ks + 1 == C::kKStages) ? 0 : ks + 1;
+        const uint32_t kph1 = (ks1 == 0) ? (kph ^ 1u) : kph;
+        const int vs1 = (vs + 1 == C::kVStages) ? 0 : vs + 1;
+        const uint32_t vph1 = (vs1 == 0) ? (vph ^ 1u) : vph;
+        const bool more = (j + 1 < nkv);
+        // PV0(j)
         if (j < nt[0]) {
           if (!wait(bar_p(0), j & 1, kSiteMmaP)) break;
           tc_fence_after();
-          issue_pv(0, j);
+          issue_pv(0, vaddr, j > 0);
           if (j == nt[0] - 1) umma_commit(bar_o(0));
         }
-        const bool next_k = (j + 1 < nkv);
-        if (next_k) {
-          if (!wait(bar_kfull(kslot(j + 1)), kphase(j + 1), kSiteMmaK)) break;
+        // S0(j+1)
+        if (more) {
+          if (!wait(bar_kfull(ks1), kph1, kSiteMmaK)) break;
           tc_fence_after();
         }
         if (j + 1 < nt[0]) {
-          issue_qk(0, j + 1);
+          issue_qk(0, sK + ks1 * C::kTileBytes);
           umma_commit(bar_s(0));
         }
+        // PV1(j)
         if (j < nt[1]) {
           if (!wait(bar_p(1), j & 1, kSiteMmaP)) break;
           tc_fence_after();
-          issue_pv(1, j);
+          issue_pv(1, vaddr, j > 0);
           if (j == nt[1] - 1) umma_commit(bar_o(1));
         }
-        umma_commit(bar_vempty(vslot(j)));
+        umma_commit(bar_vempty(vs));
+        // S1(j+1); V_{j+1} is waited for here, ahead of the next PV0
+        if (more) {
+          if (!wait(bar_vfull(vs1), vph1, kSiteMmaV)) break;
+          tc_fence_after();
+        }
         if (j + 1 < nt[1]) {
-          issue_qk(1, j + 1);
+          issue_qk(1, sK + ks1 * C::kTileBytes);
           umma_commit(bar_s(1));
         }
-        if (next_k) umma_commit(bar_kempty(kslot(j + 1)));
+        if (more) umma_commit(bar_kempty(ks1));
+        ks = ks1;
+        kph = kph1;
+        vs = vs1;
+        vph = vph1;
       }
       // every MMA issued above has completed before TMEM is released
       umma_commit(bar_done);
