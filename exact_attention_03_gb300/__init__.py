@@ -19,7 +19,7 @@ from typing import Optional, Tuple
 __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
-           "forward", "forward_host", "EXPORTED_SYMBOLS"]
+           "forward", "forward_host", "decode_noalloc", "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -43,6 +43,11 @@ _SIGS = {
     "fa_decode_num_splits": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
     "fa_wait_selftest": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p]),
     "fa_abi_version": (ctypes.c_int, []),
+    "fa_fwd_decode_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_float, ctypes.c_void_p]),
+    "fa_decode_noalloc_max_floats": (ctypes.c_int, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -141,6 +146,34 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, out=No
                 int(causal), _stream_handle(stream))
     if st != FA_OK:
         raise FlashAttentionError(st)
+    return out, lse
+
+
+def decode_noalloc(q, k, v, scale: Optional[float] = None, out=None, lse=None, stream=None):
+    """Single-query attention (q [B,H,1,D]) through fa_fwd_decode_noalloc,
+    which uses the library's fixed device array instead of allocating a
+    workspace (for callers that must not allocate while they run).  The
+    caller must not run two such calls concurrently on the GPU."""
+    import torch
+
+    B, H, Lq, D = q.shape
+    if Lq != 1:
+        raise ValueError("decode_noalloc takes one query row per head")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, H, 1, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    st = load().fa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr(), B, H, Lk, D, float(scale),
+                                      _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_fwd_decode_noalloc")
     return out, lse
 
 

@@ -106,6 +106,37 @@ int fa_decode_num_splits(int BH, int Lk, int num_sms);
  */
 int fa_wait_selftest(int limit_us, void* stream);
 
+/*
+ * fa_fwd_decode_noalloc - single-query attention (Lq = 1, non-causal) that
+ * allocates no memory.  The pages describe no such variant; it exists for
+ * callers that cannot allocate device memory while they run (an engine that
+ * plans all memory before serving, a plugin inside a framework-owned memory
+ * budget, a latency-critical loop where a memory-pool growth would stall).
+ *
+ * Arguments mean what they mean for fa_fwd with Lq = 1: q, o bf16 [B, H, 1, D],
+ * k, v bf16 [B, H, Lk, D], lse fp32 [B, H, 1] (may be NULL), D in {64, 128},
+ * finite scale > 0, all device pointers owned by the caller.
+ *
+ * Instead of a per-call workspace it uses one device array of
+ * fa_decode_noalloc_max_floats() floats (4 MiB) that the library reserves on
+ * every GPU that loads it, until the process exits.  B * H * (D + 2) must fit
+ * in it (B * H <= 8065 at D = 128), else FA_ERR_UNSUPPORTED is returned before
+ * any CUDA call; within that limit the number of key splits is capped so that
+ * the partial results fit.  No cudaMalloc/cudaFree or allocating library call
+ * is made.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  The array keeps the last call's contents; every slot a call reads
+ * is written by the same call first, so nothing needs clearing.
+ * Errors: as fa_fwd.
+ */
+int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int Lk, int D, float scale, void* stream);
+
+/* fa_decode_noalloc_max_floats - size, in floats, of fa_fwd_decode_noalloc's array. */
+int fa_decode_noalloc_max_floats(void);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
