@@ -21,6 +21,7 @@ rank 0 reports the max step time over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -46,6 +47,44 @@ def load_peaks():
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except Exception:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+PREFILL_SOURCES = ("exact_attention_03_gb300/csrc/fa_prefill_sm103.cu",
+                   "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
+DECODE_SOURCES = ("exact_attention_03_gb300/csrc/fa_decode_sm103.cu",
+                  "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
+
+
+def measured_traffic(key, sources):
+    """DRAM bytes of a kernel unit from profiles/traffic.json (ncu counters),
+    or None when the kernel sources changed since the counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entry = json.load(f)[key]
+        h = hashlib.sha256()
+        for src in sources:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+    except Exception:
+        return None
+    return entry["bytes"] if h.hexdigest() == entry["src_sha256"] else None
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest value of x over all ranks (the job's step time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(step_flops: float, step_ms: float, world: int) -> float:
+    """Whole-job TFLOPS: every rank runs the same per-GPU step (weak scaling)."""
+    return world * step_flops / (step_ms * 1e-3) / 1e12
 
 
 def sweep_workloads():
@@ -161,12 +200,9 @@ def run_ours(args, rank, world):
     n = len(calls)
     step_ms = [sum(times[i * n:(i + 1) * n]) for i in range(args.steps)]
     mean_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_step], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_step = float(t.item())
+    mean_step = max_over_ranks(mean_step, world)
     step_flops = sum(w.flops for w in ws)
-    value = world * step_flops / (mean_step * 1e-3) / 1e12
+    value = job_throughput(step_flops, mean_step, world)
     per_len = {}
     for i, w in enumerate(ws):
         ts = [times[s * n + i] for s in range(args.steps)]
@@ -193,7 +229,7 @@ def run_ours(args, rank, world):
     check()
     h2d = sum(t.numel() * t.element_size() for (_, qh, kh, vh) in host for t in (qh, kh, vh))
     d2h = sum(w.B * w.H * w.Lq * (w.D * 2 + 4) for w in ws)
-    e2e_value = world * step_flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    e2e_value = job_throughput(step_flops, max_over_ranks(statistics.mean(e2e_ms), world), world)
 
     result = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOPS", "n_gpus": world,
@@ -216,7 +252,11 @@ def run_ours(args, rank, world):
     result["roofline"] = {"kernel": "fa_prefill_kernel<64>", "bound": "tensor",
                           "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
                           "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
-                          "peak_source": f"{peak_src} bf16 burst", "traffic": None}
+                          "peak_source": f"{peak_src} bf16 burst",
+                          "per": "one step (one launch at each of the 8 sweep lengths)",
+                          "algorithmic_bytes": sum(w.bytes for w in ws),
+                          "traffic": measured_traffic("fa_prefill_kernel<64>/sweep_d64_step",
+                                                      PREFILL_SOURCES)}
     del bufs, calls, host
 
     if rank == 0 and world == 1 and not args.no_configs:
@@ -245,12 +285,16 @@ def per_config(args, fa, flush, dev, peaks, check):
                  "ms": round(ms, 5)}
         if w.Lq == 1:
             gbs = w.bytes / (ms * 1e-3) / 1e9
+            tr = measured_traffic("fa_decode_split_kernel<128>/decode_l128k_d128_b1", DECODE_SOURCES)
             entry.update({"GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                          "launches": 2})
+                          "launches": 2, "algorithmic_bytes": w.bytes,
+                          "traffic": None if tr is None else tr * w.B})
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
+            tr = (measured_traffic("fa_prefill_kernel<128>/causal_l8k_d128", PREFILL_SOURCES)
+                  if name == "causal_l8k_d128" else None)
             entry.update({"TFLOPS": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
-                          "launches": 1})
+                          "launches": 1, "algorithmic_bytes": w.bytes, "traffic": tr})
         out[name] = entry
         del q, k, v, o, lse
         torch.cuda.empty_cache()

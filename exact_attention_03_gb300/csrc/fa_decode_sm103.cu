@@ -15,7 +15,7 @@
 //     rescale of the running denominator and output by 2^(m_old - m_new),
 //     add the new terms.  The CTA's groups are merged the same way through
 //     shared memory and the split writes (m, l, unnormalised O) in fp32.
-//   fa_decode_combine_kernel  one warp per head merges the n_split partials
+//   fa_decode_combine_kernel  one CTA per head merges the n_split partials
 //     with the same rescale identity (M = max m_s, l = sum l_s 2^(m_s - M),
 //     O = sum O_s 2^(m_s - M) / l) and writes O (bf16) and LSE (fp32).
 // Exponentials are base 2: x = q.k * scale * log2(e).
@@ -30,6 +30,7 @@ namespace {
 constexpr int kDecThreads = 256;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kUnroll = 4;  // keys per group kept in flight
+constexpr int kCombThreads = 256;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 struct DecParams {
@@ -175,22 +176,34 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecP
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecParams p) {
+__global__ void __launch_bounds__(kCombThreads) fa_decode_combine_kernel(const DecParams p) {
+  // one CTA per head: warp w folds splits w, w + 8, ... (lanes over the D
+  // output dims, several splits' loads in flight), then the warps' partial
+  // sums are folded through shared memory
   constexpr int E = D / 32;  // output dims per lane
-  const int bh = int((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (bh >= p.BH) return;
+  constexpr int W = kCombThreads / 32;
+  __shared__ float red_m[W], red_l[W];
+  __shared__ float red_acc[W][D];
+  const int bh = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  float M = -INFINITY;
-  for (int s = lane; s < p.n_split; s += 32) M = fmaxf(M, p.part_ml[(size_t(s) * p.BH + bh) * 2]);
+  float m = -INFINITY;
+  for (int s = threadIdx.x; s < p.n_split; s += kCombThreads)
+    m = fmaxf(m, p.part_ml[(size_t(s) * p.BH + bh) * 2]);
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red_m[warp] = m;
+  __syncthreads();
+  float M = red_m[0];
+#pragma unroll
+  for (int w = 1; w < W; ++w) M = fmaxf(M, red_m[w]);
   const float M_safe = (M == -INFINITY) ? 0.f : M;
 
   float acc[E], L = 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s = 0; s < p.n_split; ++s) {
+#pragma unroll 4
+  for (int s = warp; s < p.n_split; s += W) {
     const size_t slot = size_t(s) * p.BH + bh;
     const float ms = p.part_ml[slot * 2 + 0];
     const float ls = p.part_ml[slot * 2 + 1];
@@ -200,12 +213,23 @@ __global__ void __launch_bounds__(256) fa_decode_combine_kernel(const DecParams 
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = fmaf(po[e], w, acc[e]);
   }
-  const float inv = 1.f / L;
-  __nv_bfloat16* orow = p.o + size_t(bh) * D + lane * E;
 #pragma unroll
-  for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<uint32_t*>(orow + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  if (lane == 0 && p.lse != nullptr) p.lse[bh] = (M + __log2f(L)) * kLn2;
+  for (int e = 0; e < E; ++e) red_acc[warp][lane * E + e] = acc[e];
+  if (lane == 0) red_l[warp] = L;
+  __syncthreads();
+  if (threadIdx.x < D / 2) {
+    const int d = 2 * threadIdx.x;
+    float L_tot = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+      L_tot += red_l[w];
+      o0 += red_acc[w][d];
+      o1 += red_acc[w][d + 1];
+    }
+    const float inv = 1.f / L_tot;
+    *reinterpret_cast<uint32_t*>(p.o + size_t(bh) * D + d) = pack_bf16x2(o0 * inv, o1 * inv);
+    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bh] = (M + __log2f(L_tot)) * kLn2;
+  }
 }
 
 template <int D>
@@ -214,9 +238,7 @@ int launch(const DecParams& p, cudaStream_t stream) {
   if (nblk > 0x7fffffffLL) return -2;
   fa_decode_split_kernel<D><<<dim3(unsigned(nblk)), dim3(kDecThreads), 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return -4;
-  const int warps_per_blk = 256 / 32;
-  const unsigned cblk = unsigned((p.BH + warps_per_blk - 1) / warps_per_blk);
-  fa_decode_combine_kernel<D><<<dim3(cblk), dim3(256), 0, stream>>>(p);
+  fa_decode_combine_kernel<D><<<dim3(unsigned(p.BH)), dim3(kCombThreads), 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
