@@ -18,11 +18,17 @@ enum WaitSite : int {
   kSiteSoftmaxS = 6,
   kSiteSoftmaxO = 7,
   kSiteSelftest = 8,
+  kSiteMmaS = 9,
 };
 
 // Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err);
+
+// Head dimension 64 (Lq >= 1): the lockstep kernel with a separate P buffer.
+int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
+                       int* err);
 
 // Single-query split-K/V path (Lq == 1).  Arguments already validated.
 // `workspace` must hold n_split * B * H * (D + 2) floats.

@@ -1,0 +1,444 @@
+// fa_prefill_d64_sm103.cu - attention forward for head dimension 64 on sm_103a.
+//
+// Same computation as fa_prefill_sm103.cu (two 128-row query tiles per CTA,
+// S = Q K^T and O += P V on the tensor cores, the online-softmax recurrence of
+// "NTU Hung-yi Lee ML 2026 Guide: Faster Generation, Part 1: Flash Attention"
+// (quidproquo.cc), "Expand: why multiplying by exp(d1 - d2) fixes it" and
+// "Expand: the correction for the output O", in base 2 with a lazily applied
+// rescale), but scheduled for D = 64, where one 128-key tile costs the softmax
+// as much time as the tensor core:
+//
+//  * P has its own TMEM columns instead of overwriting S, so the next scores
+//    S(j+1) are computed while the softmax still works on tile j: the softmax
+//    releases S as soon as it has loaded it into registers.
+//  * Both query tiles advance in lockstep: per key tile j the MMA thread issues
+//    S0(j+1) S1(j+1) (one 512-cycle group), then, once both P(j) are written,
+//    PV0(j) PV1(j).  Every barrier wait of the MMA thread therefore sits behind
+//    a long queued group (a wait stalls that thread for a few hundred cycles).
+//  * K_j and V_j share one ring slot and one "full" barrier (two producer
+//    warps, one TMA box each).
+//
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
+//                     P0 [384,448) P1 [448,512)  (P: bf16 pairs, 128 keys)
+// Warps: 0 = TMA producer for Q and K, 1 = TMEM allocation + MMA issue,
+// 2 = TMA producer for V, 3 = idle, 4-7 = softmax of Q0, 8-11 = softmax of Q1.
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 384;
+// 128 threads x 80 + 256 threads x 208 = 63488 <= 384 x 168 registers at launch
+constexpr uint32_t kRegsCtl = 80;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr int kD = 64;
+constexpr int kTileBytes = 128 * kD * 2;       // one 128-row tile, one TMA box (16 KB)
+constexpr int kStages = 5;                     // K/V slot pairs
+constexpr int kQOff = 0;
+constexpr int kKVOff = 2 * kTileBytes;         // slot s: K at +2s tiles, V at +2s+1 tiles
+constexpr int kBarOff = kKVOff + kStages * 2 * kTileBytes;
+constexpr int kBarQ = 0;
+constexpr int kBarKVFull = 16;
+constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;
+constexpr int kBarS = kBarKVEmpty + 8 * kStages;   // S(j) of both tiles written
+constexpr int kBarSFree = kBarS + 8;               // both softmax groups loaded S(j)
+constexpr int kBarP = kBarSFree + 8;               // both P(j) written (O rescaled)
+constexpr int kBarPV = kBarP + 8;                  // PV(j) of both tiles completed
+constexpr int kBarDone = kBarPV + 8;
+constexpr int kTmemHolder = kBarDone + 8;
+constexpr int kAbort = kTmemHolder + 4;
+constexpr int kMiscBytes = 256;
+static_assert(kAbort + 4 <= kMiscBytes, "barrier area overflow");
+constexpr int kSmemBytes = kBarOff + kMiscBytes + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColO = 256;
+constexpr uint32_t kColP = 384;
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  int* err;
+  int BH, Lq, Lk;
+  int n_qblk;  // ceil(Lq / 256)
+  int causal;
+  float scale_log2;
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > 50000000ull) return;  // 50 ms
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const uint32_t sQ = base + kQOff;
+  const uint32_t sKV = base + kKVOff;
+  const uint32_t sBar = base + kBarOff;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + kBarOff + kTmemHolder);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kBarOff + kAbort);
+
+  auto bar_q = [&](int t) { return sBar + kBarQ + 8 * t; };
+  auto bar_kvfull = [&](int s) { return sBar + kBarKVFull + 8 * s; };
+  auto bar_kvempty = [&](int s) { return sBar + kBarKVEmpty + 8 * s; };
+  const uint32_t bar_s = sBar + kBarS;
+  const uint32_t bar_sfree = sBar + kBarSFree;
+  const uint32_t bar_p = sBar + kBarP;
+  const uint32_t bar_pv = sBar + kBarPV;
+  const uint32_t bar_done = sBar + kBarDone;
+  auto slot_k = [&](int s) { return sKV + (2 * s) * kTileBytes; };
+  auto slot_v = [&](int s) { return sKV + (2 * s + 1) * kTileBytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which query tiles this CTA owns (heaviest query blocks first)
+  const int qblk = p.n_qblk - 1 - int(blockIdx.x) / p.BH;
+  const int bh = int(blockIdx.x) % p.BH;
+  const int q0 = qblk * 256;
+  const int nk_all = (p.Lk + 127) / 128;
+  int nt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = q0 + 128 * t;
+    if (qt >= p.Lq) {
+      nt[t] = 0;
+    } else if (p.causal) {
+      nt[t] = min(nk_all, min(qt + 127, p.Lq - 1) / 128 + 1);
+    } else {
+      nt[t] = nk_all;
+    }
+  }
+  const int nkv = max(nt[0], nt[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q(0), 1);
+    mbar_init(bar_q(1), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_kvfull(s), 2);  // the K and the V producer each arrive (with bytes)
+      mbar_init(bar_kvempty(s), 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_sfree, 256);
+    mbar_init(bar_p, 256);
+    mbar_init(bar_pv, 1);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int wgrp = __shfl_sync(0xffffffffu, int(threadIdx.x) / 128, 0);
+
+  if (wgrp == 0) {
+    setmaxnreg_dec<kRegsCtl>();
+    if (warp == 0 || warp == 2) {
+      // =================== TMA producers (warp 0: Q and K, warp 2: V) ===================
+      if (lane == 0) {
+        const bool is_k = (warp == 0);
+        if (is_k) {
+          mbar_arrive_expect_tx(bar_q(0), kTileBytes);
+          tma_load_tile(sQ, &tmQ, bar_q(0), q0, bh);
+          if (nt[1] > 0) {
+            mbar_arrive_expect_tx(bar_q(1), kTileBytes);
+            tma_load_tile(sQ + kTileBytes, &tmQ, bar_q(1), q0 + 128, bh);
+          }
+        }
+        int issued = 0;
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j % kStages;
+          const int use = j / kStages;
+          if (!mbar_wait(bar_kvempty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
+          mbar_arrive_expect_tx(bar_kvfull(s), kTileBytes);
+          tma_load_tile(is_k ? slot_k(s) : slot_v(s), is_k ? &tmK : &tmV, bar_kvfull(s), j * 128, bh);
+          ++issued;
+        }
+        if (is_k) {
+          drain_wait(bar_q(0), 0);
+          if (nt[1] > 0) drain_wait(bar_q(1), 0);
+        }
+        for (int s = 0; s < kStages && s < issued; ++s) {
+          const int last = s + kStages * ((issued - 1 - s) / kStages);
+          drain_wait(bar_kvfull(s), (last / kStages) & 1);
+        }
+      }
+    } else if (warp == 1) {
+      // =================== MMA issuer ===================
+      if (lane == 0) {
+        constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
+        constexpr uint32_t kIdPV = idesc_bf16_f32(128, kD, false, true);
+        constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);      // Q, K: K-major
+        constexpr uint64_t kDescMN = sdesc_sw128(0, 16, 1024);     // V: MN-major, one 64-col block
+        bool ok = true;
+        auto wait = [&](uint32_t b, uint32_t ph, int site) {
+          if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
+          return ok;
+        };
+        // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = 64 in steps of 16
+        auto issue_qk = [&](int t, uint32_t kaddr) {
+          const uint32_t a0 = sQ + t * kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + kk * 32), sdesc_at(kDescK, kaddr + kk * 32),
+                    kIdQK, kk > 0 ? 1u : 0u);
+        };
+        // O_t += P_t V: M = 128 rows, N = 64, K = 128 keys in steps of 16
+        auto issue_pv = [&](int t, uint32_t vaddr, bool accumulate) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + kColO + t * kD, tmem + kColP + t * 64 + kk * 8,
+                    sdesc_at(kDescMN, vaddr + kk * 16 * 128), kIdPV, (accumulate || kk > 0) ? 1u : 0u);
+        };
+
+        wait(bar_q(0), 0, kSiteMmaQ);
+        if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
+        if (wait(bar_kvfull(0), 0, kSiteMmaK)) {
+          tc_fence_after();
+          if (nt[0] > 0) issue_qk(0, slot_k(0));
+          if (nt[1] > 0) issue_qk(1, slot_k(0));
+          umma_commit(bar_s);
+        }
+        int sc = 0;          // ring slot of K_j / V_j
+        uint32_t phc = 0;    // and its phase
+        for (int j = 0; j < nkv && ok; ++j) {
+          const int sn = (sc + 1 == kStages) ? 0 : sc + 1;
+          const uint32_t phn = (sn == 0) ? (phc ^ 1u) : phc;
+          // S(j+1) as soon as both softmax groups hold S(j) in registers
+          if (j + 1 < nkv) {
+            if (!wait(bar_kvfull(sn), phn, kSiteMmaK)) break;
+            if (!wait(bar_sfree, j & 1, kSiteMmaS)) break;
+            tc_fence_after();
+            if (j + 1 < nt[0]) issue_qk(0, slot_k(sn));
+            if (j + 1 < nt[1]) issue_qk(1, slot_k(sn));
+            umma_commit(bar_s);
+          }
+          // PV(j) once both P(j) are written
+          if (!wait(bar_p, j & 1, kSiteMmaP)) break;
+          tc_fence_after();
+          if (j < nt[0]) issue_pv(0, slot_v(sc), j > 0);
+          if (j < nt[1]) issue_pv(1, slot_v(sc), j > 0);
+          umma_commit(bar_pv);
+          umma_commit(bar_kvempty(sc));
+          sc = sn;
+          phc = phn;
+        }
+        umma_commit(bar_done);
+        drain_wait(bar_done, 0);
+      }
+    }
+  } else {
+    setmaxnreg_inc<kRegsSoftmax>();
+    // =================== softmax + epilogue (one query row per thread) ===================
+    const int t = (warp - 4) >> 2;
+    const int g = warp & 3;
+    const int r = g * 32 + lane;
+    const int qt = q0 + 128 * t;
+    const int qrow = qt + r;
+    const uint32_t lane_off = uint32_t(g * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tP = tmem + lane_off + kColP + t * 64;
+    const uint32_t tO = tmem + lane_off + kColO + t * kD;
+    const float c = p.scale_log2;
+    const int n = t ? nt[1] : nt[0];
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+
+    // every iteration arrives on s_free and p_full (the MMA thread counts all
+    // 256 softmax threads), also past this tile's last key tile
+    for (int j = 0; j < nkv; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      const bool act = (j < n);
+      float s[128];
+      if (act) {
+        tc_fence_after();
+        tmem_ld128_sync(tS, s);
+      }
+      tc_fence_before();
+      mbar_arrive(bar_sfree);  // S_t(j) is in registers: S_t may be overwritten
+
+      float alpha = 1.f;
+      bool any = false;
+      uint32_t pk[32];   // P of keys 0-63, computed before PV(j-1) has freed P_t
+      float2 acc[4];
+      float2 c2 = make_float2(0.f, 0.f), nm2 = make_float2(0.f, 0.f);
+      if (act) {
+        const int k0 = j * 128;
+        const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
+        if (edge) {
+          const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i >= lim) s[i] = -INFINITY;
+        }
+        float pm[16];
+#pragma unroll
+        for (int g2 = 0; g2 < 16; ++g2) {
+          float a = fmax3(s[8 * g2], s[8 * g2 + 1], s[8 * g2 + 2]);
+          a = fmax3(a, s[8 * g2 + 3], s[8 * g2 + 4]);
+          a = fmax3(a, s[8 * g2 + 5], s[8 * g2 + 6]);
+          pm[g2] = fmaxf(a, s[8 * g2 + 7]);
+        }
+        const float mx = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                                     fmax3(pm[6], pm[7], pm[8])),
+                               fmax3(pm[9], pm[10], pm[11]),
+                               fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
+        const float m_cand = fmaxf(m_run, mx * c);
+        const bool need = (m_cand - m_run) > kRescaleLog2;
+        any = __any_sync(0xffffffffu, need);
+        const float m_use = any ? m_cand : m_run;
+        const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
+        alpha = ex2_approx(m_run - m_safe);
+        m_run = m_use;
+        c2 = make_float2(c, c);
+        nm2 = make_float2(-m_safe, -m_safe);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          pk[i] = pack_bf16x2(pr.x, pr.y);
+        }
+      }
+
+      // PV(j-1) has completed: O_t is stable and P_t is free
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
+        if (!ok) break;
+      }
+      if (act) {
+        tc_fence_after();
+        if (any && j > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < kD; cc += 16) {
+            float ov[16];
+            tmem_ld16_sync(tO + cc, ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(ov[i] * alpha);
+            tmem_st16(tO + cc, w);
+          }
+        }
+#pragma unroll
+        for (int cb = 0; cb < 2; ++cb) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pk[16 * cb + i];
+          tmem_st16(tP + 16 * cb, w);
+        }
+        // keys 64-127: computed and stored now that P_t is free
+#pragma unroll
+        for (int cb = 2; cb < 4; ++cb) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int e = 32 * cb + 2 * i;
+            const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
+            const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+            w[i] = pack_bf16x2(pr.x, pr.y);
+          }
+          tmem_st16(tP + 16 * cb, w);
+        }
+        const float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        l_run = l_run * alpha + (a03.x + a03.y);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+
+    // epilogue: wait for the last PV, then O / l -> bf16, LSE
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (nkv - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
+    if (ok && n > 0) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      const bool valid = qrow < p.Lq;
+      __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * kD;
+#pragma unroll 1
+      for (int cc = 0; cc < kD; cc += 32) {
+        float ov[32];
+        tmem_ld32_sync(tO + cc, ov);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+      if (valid && p.lse != nullptr) p.lse[size_t(bh) * p.Lq + qrow] = (m_run + __log2f(l_run)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
+                       int* err) {
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  int st = make_tensor_map_bf16(&mq, q, BH, Lq, kD);
+  if (st == 0) st = make_tensor_map_bf16(&mk, k, BH, Lk, kD);
+  if (st == 0) st = make_tensor_map_bf16(&mv, v, BH, Lk, kD);
+  if (st != 0) return st;
+  Params p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.err = err;
+  p.BH = BH;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.n_qblk = (Lq + 255) / 256;
+  p.causal = causal;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  if (cudaFuncSetAttribute(fa_prefill_d64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return -4;
+  const long long nblk = (long long)p.n_qblk * BH;
+  if (nblk > 0x7fffffffLL) return -2;
+  fa_prefill_d64_kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace fa
