@@ -1,4 +1,5 @@
-// fa_prefill_sm103.cu - attention forward for Lq >= 1 on sm_103a.
+// fa_prefill_sm103.cu - attention forward for Lq >= 1 on sm_103a (head dimension 128;
+// head dimension 64 dispatches to fa_prefill_d64_sm103.cu).
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
 // streams that head's K/V in 128-key tiles through a shared-memory ring.
@@ -508,7 +509,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err) {
-  if (D == 64) return launch<64>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
+  if (D == 64) return launch_prefill_d64(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
   if (D == 128) return launch<128>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
   return -2;
 }
