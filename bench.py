@@ -51,6 +51,8 @@ def load_peaks():
 
 PREFILL_SOURCES = ("exact_attention_03_gb300/csrc/fa_prefill_sm103.cu",
                    "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
+PREFILL_D64_SOURCES = ("exact_attention_03_gb300/csrc/fa_prefill_d64_sm103.cu",
+                       "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
 DECODE_SOURCES = ("exact_attention_03_gb300/csrc/fa_decode_sm103.cu",
                   "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
 
@@ -249,14 +251,14 @@ def run_ours(args, rank, world):
     }
     prefill_ms = mean_step  # every launch of the step is the prefill kernel
     achieved = step_flops / (prefill_ms * 1e-3) / 1e12
-    result["roofline"] = {"kernel": "fa_prefill_kernel<64>", "bound": "tensor",
+    result["roofline"] = {"kernel": "fa_prefill_d64_kernel", "bound": "tensor",
                           "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
                           "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                           "peak_source": f"{peak_src} bf16 burst",
                           "per": "one step (one launch at each of the 8 sweep lengths)",
                           "algorithmic_bytes": sum(w.bytes for w in ws),
-                          "traffic": measured_traffic("fa_prefill_kernel<64>/sweep_d64_step",
-                                                      PREFILL_SOURCES)}
+                          "traffic": measured_traffic("fa_prefill_d64_kernel/sweep_d64_step",
+                                                      PREFILL_D64_SOURCES)}
     del bufs, calls, host
 
     if rank == 0 and world == 1 and not args.no_configs:
