@@ -35,6 +35,7 @@ constexpr int kThreads = 384;
 constexpr uint32_t kRegsCtl = 80;
 constexpr uint32_t kRegsSoftmax = 208;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr float kRescaleBound = 256.0f;        // 2^kRescaleLog2
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr int kD = 64;
 constexpr int kTileBytes = 128 * kD * 2;       // one 128-row tile, one TMA box (16 KB)
@@ -75,6 +76,20 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return;
     if ((it & 15u) == 15u && globaltimer_ns() - t0 > 50000000ull) return;  // 50 ms
   }
+}
+
+// maximum of a 128-key score row (3-input max tree)
+__device__ __forceinline__ float row_max128(const float (&s)[128]) {
+  float pm[16];
+#pragma unroll
+  for (int g2 = 0; g2 < 16; ++g2) {
+    float a = fmax3(s[8 * g2], s[8 * g2 + 1], s[8 * g2 + 2]);
+    a = fmax3(a, s[8 * g2 + 3], s[8 * g2 + 4]);
+    a = fmax3(a, s[8 * g2 + 5], s[8 * g2 + 6]);
+    pm[g2] = fmaxf(a, s[8 * g2 + 7]);
+  }
+  return fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]), fmax3(pm[6], pm[7], pm[8])),
+               fmax3(pm[9], pm[10], pm[11]), fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -284,10 +299,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar_sfree);  // S_t(j) is in registers: S_t may be overwritten
 
       float alpha = 1.f;
-      bool any = false;
-      uint32_t pk[32];   // P of keys 0-63, computed before PV(j-1) has freed P_t
+      bool resc = false;    // warp-uniform: O_t is multiplied by alpha before PV(j)
+      bool exact = false;   // warp-uniform: the tile maximum was taken before the exponentials
       float2 acc[4];
-      float2 c2 = make_float2(0.f, 0.f), nm2 = make_float2(0.f, 0.f);
+      const float2 c2 = make_float2(c, c);
+      float2 nm2 = make_float2(0.f, 0.f);
+      // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
+      auto exp_block = [&](int cb, uint32_t (&w)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = 32 * cb + 2 * i;
+          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          w[i] = pack_bf16x2(pr.x, pr.y);
+        }
+      };
+      auto rescale_o = [&]() {
+#pragma unroll 1
+        for (int cc = 0; cc < kD; cc += 16) {
+          float ov[16];
+          tmem_ld16_sync(tO + cc, ov);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(ov[i] * alpha);
+          tmem_st16(tO + cc, w);
+        }
+      };
+      uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P_t
       if (act) {
         const int k0 = j * 128;
         const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
@@ -297,36 +336,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (i >= lim) s[i] = -INFINITY;
         }
-        float pm[16];
-#pragma unroll
-        for (int g2 = 0; g2 < 16; ++g2) {
-          float a = fmax3(s[8 * g2], s[8 * g2 + 1], s[8 * g2 + 2]);
-          a = fmax3(a, s[8 * g2 + 3], s[8 * g2 + 4]);
-          a = fmax3(a, s[8 * g2 + 5], s[8 * g2 + 6]);
-          pm[g2] = fmaxf(a, s[8 * g2 + 7]);
+        // Until a row has a finite running maximum its first tile takes the
+        // maximum before exponentiating; later tiles exponentiate against the
+        // running maximum and check the result afterwards (below).
+        exact = __any_sync(0xffffffffu, m_run == -INFINITY);
+        if (exact) {
+          const float m_cand = fmaxf(m_run, row_max128(s) * c);
+          resc = __any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2);
+          if (resc) {
+            alpha = ex2_approx(m_run - ((m_cand == -INFINITY) ? 0.f : m_cand));
+            m_run = m_cand;
+          }
         }
-        const float mx = fmax3(fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                                     fmax3(pm[6], pm[7], pm[8])),
-                               fmax3(pm[9], pm[10], pm[11]),
-                               fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
-        const float m_cand = fmaxf(m_run, mx * c);
-        const bool need = (m_cand - m_run) > kRescaleLog2;
-        any = __any_sync(0xffffffffu, need);
-        const float m_use = any ? m_cand : m_run;
-        const float m_safe = (m_use == -INFINITY) ? 0.f : m_use;
-        alpha = ex2_approx(m_run - m_safe);
-        m_run = m_use;
-        c2 = make_float2(c, c);
+        const float m_safe = (m_run == -INFINITY) ? 0.f : m_run;
         nm2 = make_float2(-m_safe, -m_safe);
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2, nm2);
-          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
-          pk[i] = pack_bf16x2(pr.x, pr.y);
-        }
+        exp_block(0, pk[0]);
+        exp_block(1, pk[1]);
       }
 
       // PV(j-1) has completed: O_t is stable and P_t is free
@@ -336,39 +363,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (act) {
         tc_fence_after();
-        if (any && j > 0) {
-#pragma unroll 1
-          for (int cc = 0; cc < kD; cc += 16) {
-            float ov[16];
-            tmem_ld16_sync(tO + cc, ov);
-            uint32_t w[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(ov[i] * alpha);
-            tmem_st16(tO + cc, w);
-          }
-        }
-#pragma unroll
-        for (int cb = 0; cb < 2; ++cb) {
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = pk[16 * cb + i];
-          tmem_st16(tP + 16 * cb, w);
-        }
+        if (resc && j > 0) rescale_o();
+        tmem_st16(tP, pk[0]);
+        tmem_st16(tP + 16, pk[1]);
         // keys 64-127: computed and stored now that P_t is free
 #pragma unroll
         for (int cb = 2; cb < 4; ++cb) {
           uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int e = 32 * cb + 2 * i;
-            const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
-            const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
-            w[i] = pack_bf16x2(pr.x, pr.y);
-          }
+          exp_block(cb, w);
           tmem_st16(tP + 16 * cb, w);
         }
-        const float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        if (!exact) {
+          // Every weight 2^(c s - m_run) is at most the tile's row sum, so a sum
+          // up to 2^kRescaleLog2 means the maximum grew by at most kRescaleLog2
+          // and the weights stand (the lazy rescale rule).  Otherwise take the
+          // maximum, and where it grew further, rescale and recompute the tile.
+          const bool check = !(a03.x + a03.y <= kRescaleBound);
+          if (__any_sync(0xffffffffu, check)) {
+            const float m_cand = fmaxf(m_run, row_max128(s) * c);
+            if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2)) {
+              alpha = ex2_approx(m_run - m_cand);
+              m_run = m_cand;
+              nm2 = make_float2(-m_cand, -m_cand);
+#pragma unroll
+              for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int cb = 0; cb < 4; ++cb) {
+                uint32_t w[16];
+                exp_block(cb, w);
+                tmem_st16(tP + 16 * cb, w);
+              }
+              a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+              if (j > 0) rescale_o();
+            }
+          }
+        }
         l_run = l_run * alpha + (a03.x + a03.y);
         tmem_st_wait();
       }

@@ -137,15 +137,37 @@ def test_sharp_logits(D, causal):
     assert_parity(q, k, v, causal)
 
 
-def test_late_outliers_force_rescale():
+@pytest.mark.parametrize("D", [64, 128])
+def test_late_outliers_force_rescale(D):
     # large keys placed only at the end of the sequence: the running max keeps
     # growing tile after tile
-    w = Workload("late", 1, 2, 512, 1536, 128, False, seed=11)
+    w = Workload("late", 1, 2, 512, 1536, D, False, seed=11)
     q, k, v = make_inputs(w, "cpu")
     k = k.clone()
     k[:, :, 1024:] = (k[:, :, 1024:].float() * 6).to(torch.bfloat16)
     q, k, v = _dev(q, k, v)
     assert_parity(q, k, v, False)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_running_max_growth_per_tile(D):
+    # scale = ln 2 makes the base-2 logit equal to q.k.  q = (1, 0.1 n): key
+    # tile 0 scores ~0, tile 1 ~1.5 (its weights against the old maximum sum
+    # past 2^8 although no weight grows past 2^8), tile 2 ~12 (a growth past
+    # 2^8 after the first tile: rescale O and recompute the tile), tile 3
+    # back to ~0, and a ragged tile 4.
+    g = torch.Generator().manual_seed(21)
+    B, H, Lq, Lk = 1, 2, 600, 600
+    q = torch.randn(B, H, Lq, D, generator=g) * 0.1
+    q[..., 0] = 1.0
+    k = torch.randn(B, H, Lk, D, generator=g)
+    k[..., 0] = 0.0
+    k[:, :, 128:256, 0] = 1.5
+    k[:, :, 256:384, 0] = 12.0
+    v = torch.randn(B, H, Lk, D, generator=g)
+    q, k, v = _dev(*(t.to(torch.bfloat16) for t in (q, k, v)))
+    assert_parity(q, k, v, False, scale=math.log(2.0))
+    assert_parity(q, k, v, True, scale=math.log(2.0))
 
 
 def test_custom_scale():
