@@ -19,13 +19,15 @@ enum WaitSite : int {
   kSiteSoftmaxO = 7,
   kSiteSelftest = 8,
   kSiteMmaS = 9,
+  kSiteSoftmaxGo = 10,
 };
 
 // Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err);
 
-// Head dimension 64 (Lq >= 1): the lockstep kernel with a separate P buffer.
+// Head dimension 64 (Lq >= 1): separate P buffer, one MMA issuer per query tile,
+// the two query tiles' softmax groups half an iteration apart.
 int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
                        int* err);

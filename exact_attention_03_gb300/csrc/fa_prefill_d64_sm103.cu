@@ -6,22 +6,27 @@
 // (quidproquo.cc), "Expand: why multiplying by exp(d1 - d2) fixes it" and
 // "Expand: the correction for the output O", in base 2 with a lazily applied
 // rescale), but scheduled for D = 64, where one 128-key tile costs the softmax
-// as much time as the tensor core:
+// (MUFU exponentials) about as much time as the tensor core:
 //
 //  * P has its own TMEM columns instead of overwriting S, so the next scores
 //    S(j+1) are computed while the softmax still works on tile j: the softmax
 //    releases S as soon as it has loaded it into registers.
-//  * Both query tiles advance in lockstep: per key tile j the MMA thread issues
-//    S0(j+1) S1(j+1) (one 512-cycle group), then, once both P(j) are written,
-//    PV0(j) PV1(j).  Every barrier wait of the MMA thread therefore sits behind
-//    a long queued group (a wait stalls that thread for a few hundred cycles).
+//  * Each query tile has its own pipeline: its own MMA-issuing thread (warp 1
+//    for tile 0, warp 3 for tile 1), barriers, S, P and O.  The two pipelines
+//    share only the K/V ring and the tensor core, and their softmax groups run
+//    about half an iteration apart (the second starts once the first has its
+//    first half tile of weights), so that one group's TMEM loads, barrier waits
+//    and the drain of its exponentials overlap the other's exponentials.
+//  * Exponentials are taken against the running maximum and checked
+//    afterwards; the row maximum is computed only when the check fails.
 //  * K_j and V_j share one ring slot and one "full" barrier (two producer
 //    warps, one TMA box each).
 //
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,320) O1 [320,384)
 //                     P0 [384,448) P1 [448,512)  (P: bf16 pairs, 128 keys)
-// Warps: 0 = TMA producer for Q and K, 1 = TMEM allocation + MMA issue,
-// 2 = TMA producer for V, 3 = idle, 4-7 = softmax of Q0, 8-11 = softmax of Q1.
+// Warps: 0 = TMA producer for Q and K, 1 = TMEM allocation + MMA issue for Q0,
+// 2 = TMA producer for V, 3 = MMA issue for Q1, 4-7 = softmax of Q0,
+// 8-11 = softmax of Q1.
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -46,12 +51,13 @@ constexpr int kBarOff = kKVOff + kStages * 2 * kTileBytes;
 constexpr int kBarQ = 0;
 constexpr int kBarKVFull = 16;
 constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;
-constexpr int kBarS = kBarKVEmpty + 8 * kStages;   // S(j) of both tiles written
-constexpr int kBarSFree = kBarS + 8;               // both softmax groups loaded S(j)
-constexpr int kBarP = kBarSFree + 8;               // both P(j) written (O rescaled)
-constexpr int kBarPV = kBarP + 8;                  // PV(j) of both tiles completed
-constexpr int kBarDone = kBarPV + 8;
-constexpr int kTmemHolder = kBarDone + 8;
+constexpr int kBarS = kBarKVEmpty + 8 * kStages;   // [t] S_t(j) written
+constexpr int kBarSFree = kBarS + 16;              // [t] softmax group t loaded S_t(j)
+constexpr int kBarP = kBarSFree + 16;              // [t] P_t(j) written (O_t rescaled)
+constexpr int kBarPV = kBarP + 16;                 // [t] PV_t(j) completed
+constexpr int kBarGo = kBarPV + 16;                // group 0 is half a tile ahead
+constexpr int kBarDone = kBarGo + 8;               // [t] all MMAs of issuer t completed
+constexpr int kTmemHolder = kBarDone + 16;
 constexpr int kAbort = kTmemHolder + 4;
 constexpr int kMiscBytes = 256;
 static_assert(kAbort + 4 <= kMiscBytes, "barrier area overflow");
@@ -110,10 +116,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_q = [&](int t) { return sBar + kBarQ + 8 * t; };
   auto bar_kvfull = [&](int s) { return sBar + kBarKVFull + 8 * s; };
   auto bar_kvempty = [&](int s) { return sBar + kBarKVEmpty + 8 * s; };
-  const uint32_t bar_s = sBar + kBarS;
-  const uint32_t bar_sfree = sBar + kBarSFree;
-  const uint32_t bar_p = sBar + kBarP;
-  const uint32_t bar_pv = sBar + kBarPV;
+  auto bar_s = [&](int t) { return sBar + kBarS + 8 * t; };
+  auto bar_sfree = [&](int t) { return sBar + kBarSFree + 8 * t; };
+  auto bar_p = [&](int t) { return sBar + kBarP + 8 * t; };
+  auto bar_pv = [&](int t) { return sBar + kBarPV + 8 * t; };
+  const uint32_t bar_go = sBar + kBarGo;
   const uint32_t bar_done = sBar + kBarDone;
   auto slot_k = [&](int s) { return sKV + (2 * s) * kTileBytes; };
   auto slot_v = [&](int s) { return sKV + (2 * s + 1) * kTileBytes; };
@@ -126,32 +133,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = int(blockIdx.x) % p.BH;
   const int q0 = qblk * 256;
   const int nk_all = (p.Lk + 127) / 128;
-  int nt[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int qt = q0 + 128 * t;
-    if (qt >= p.Lq) {
-      nt[t] = 0;
-    } else if (p.causal) {
-      nt[t] = min(nk_all, min(qt + 127, p.Lq - 1) / 128 + 1);
-    } else {
-      nt[t] = nk_all;
-    }
-  }
-  const int nkv = max(nt[0], nt[1]);
+  // key tiles of query tile 0 and 1; nt0 >= 1, and nt1 is 0 (tile 1 past the
+  // end of the sequence) or nt1 >= nt0
+  const int nt0 = p.causal ? min(nk_all, min(q0 + 127, p.Lq - 1) / 128 + 1) : nk_all;
+  const int nt1 = (q0 + 128 >= p.Lq) ? 0
+                  : (p.causal ? min(nk_all, min(q0 + 255, p.Lq - 1) / 128 + 1) : nk_all);
+  const int nkv = max(nt0, nt1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q(0), 1);
     mbar_init(bar_q(1), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_kvfull(s), 2);  // the K and the V producer each arrive (with bytes)
-      mbar_init(bar_kvempty(s), 1);
+      mbar_init(bar_kvempty(s), nt1 > 0 ? 2 : 1);  // each MMA issuer commits once per key tile
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_sfree, 256);
-    mbar_init(bar_p, 256);
-    mbar_init(bar_pv, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s(t), 1);
+      mbar_init(bar_sfree(t), 128);
+      mbar_init(bar_p(t), 128);
+      mbar_init(bar_pv(t), 1);
+    }
+    mbar_init(bar_go, 128);
     mbar_init(bar_done, 1);
+    mbar_init(bar_done + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (is_k) {
           mbar_arrive_expect_tx(bar_q(0), kTileBytes);
           tma_load_tile(sQ, &tmQ, bar_q(0), q0, bh);
-          if (nt[1] > 0) {
+          if (nt1 > 0) {
             mbar_arrive_expect_tx(bar_q(1), kTileBytes);
             tma_load_tile(sQ + kTileBytes, &tmQ, bar_q(1), q0 + 128, bh);
           }
@@ -195,16 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (is_k) {
           drain_wait(bar_q(0), 0);
-          if (nt[1] > 0) drain_wait(bar_q(1), 0);
+          if (nt1 > 0) drain_wait(bar_q(1), 0);
         }
         for (int s = 0; s < kStages && s < issued; ++s) {
           const int last = s + kStages * ((issued - 1 - s) / kStages);
           drain_wait(bar_kvfull(s), (last / kStages) & 1);
         }
       }
-    } else if (warp == 1) {
-      // =================== MMA issuer ===================
+    } else if (warp == 1 || (warp == 3 && nt1 > 0)) {
+      // =================== MMA issuers: warp 1 for query tile 0, warp 3 for tile 1 ===================
       if (lane == 0) {
+        const int t = (warp == 1) ? 0 : 1;
+        const int n = t ? nt1 : nt0;
         constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
         constexpr uint32_t kIdPV = idesc_bf16_f32(128, kD, false, true);
         constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);      // Q, K: K-major
@@ -214,56 +220,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
           return ok;
         };
-        // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = 64 in steps of 16
-        auto issue_qk = [&](int t, uint32_t kaddr) {
-          const uint32_t a0 = sQ + t * kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + kk * 32), sdesc_at(kDescK, kaddr + kk * 32),
-                    kIdQK, kk > 0 ? 1u : 0u);
-        };
-        // O_t += P_t V: M = 128 rows, N = 64, K = 128 keys in steps of 16
-        auto issue_pv = [&](int t, uint32_t vaddr, bool accumulate) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + kColO + t * kD, tmem + kColP + t * 64 + kk * 8,
-                    sdesc_at(kDescMN, vaddr + kk * 16 * 128), kIdPV, (accumulate || kk > 0) ? 1u : 0u);
-        };
-
-        wait(bar_q(0), 0, kSiteMmaQ);
-        if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
-        if (wait(bar_kvfull(0), 0, kSiteMmaK)) {
-          tc_fence_after();
-          if (nt[0] > 0) issue_qk(0, slot_k(0));
-          if (nt[1] > 0) issue_qk(1, slot_k(0));
-          umma_commit(bar_s);
-        }
-        int sc = 0;          // ring slot of K_j / V_j
-        uint32_t phc = 0;    // and its phase
-        for (int j = 0; j < nkv && ok; ++j) {
-          const int sn = (sc + 1 == kStages) ? 0 : sc + 1;
-          const uint32_t phn = (sn == 0) ? (phc ^ 1u) : phc;
-          // S(j+1) as soon as both softmax groups hold S(j) in registers
-          if (j + 1 < nkv) {
-            if (!wait(bar_kvfull(sn), phn, kSiteMmaK)) break;
-            if (!wait(bar_sfree, j & 1, kSiteMmaS)) break;
+        const uint32_t a0 = sQ + t * kTileBytes;
+        wait(bar_q(t), 0, kSiteMmaQ);
+        for (int j = 0; j <= nkv && ok; ++j) {
+          const int sc = j % kStages;
+          if (j < nkv && !wait(bar_kvfull(sc), (j / kStages) & 1, kSiteMmaK)) break;
+          // S_t(j) once the softmax group holds S_t(j-1) in registers
+          if (j < n) {
+            if (j > 0 && !wait(bar_sfree(t), (j - 1) & 1, kSiteMmaS)) break;
             tc_fence_after();
-            if (j + 1 < nt[0]) issue_qk(0, slot_k(sn));
-            if (j + 1 < nt[1]) issue_qk(1, slot_k(sn));
-            umma_commit(bar_s);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + kk * 32), sdesc_at(kDescK, slot_k(sc) + kk * 32),
+                      kIdQK, kk > 0 ? 1u : 0u);
+            umma_commit(bar_s(t));
           }
-          // PV(j) once both P(j) are written
-          if (!wait(bar_p, j & 1, kSiteMmaP)) break;
-          tc_fence_after();
-          if (j < nt[0]) issue_pv(0, slot_v(sc), j > 0);
-          if (j < nt[1]) issue_pv(1, slot_v(sc), j > 0);
-          umma_commit(bar_pv);
-          umma_commit(bar_kvempty(sc));
-          sc = sn;
-          phc = phn;
+          // PV_t(j-1) once P_t(j-1) is written; then this issuer is done with slot j-1
+          if (j > 0) {
+            const int sp = (j - 1) % kStages;
+            if (j - 1 < n) {
+              if (!wait(bar_p(t), (j - 1) & 1, kSiteMmaP)) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_ts(tmem + kColO + t * kD, tmem + kColP + t * 64 + kk * 8,
+                        sdesc_at(kDescMN, slot_v(sp) + kk * 16 * 128), kIdPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              umma_commit(bar_pv(t));
+            }
+            umma_commit(bar_kvempty(sp));
+          }
         }
-        umma_commit(bar_done);
-        drain_wait(bar_done, 0);
+        umma_commit(bar_done + 8 * t);
+        drain_wait(bar_done + 8 * t, 0);
       }
     }
   } else {
@@ -279,28 +267,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tP = tmem + lane_off + kColP + t * 64;
     const uint32_t tO = tmem + lane_off + kColO + t * kD;
     const float c = p.scale_log2;
-    const int n = t ? nt[1] : nt[0];
+    const int n = t ? nt1 : nt0;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
 
-    // every iteration arrives on s_free and p_full (the MMA thread counts all
-    // 256 softmax threads), also past this tile's last key tile
-    for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.err, kSiteSoftmaxS));
+    // group 1 starts once group 0 has its first half tile of weights
+    if (t == 1 && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_go, 0, abort_flag, p.err, kSiteSoftmaxGo));
+
+    for (int j = 0; j < n && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
-      const bool act = (j < n);
       float s[128];
-      if (act) {
-        tc_fence_after();
-        tmem_ld128_sync(tS, s);
-      }
+      tc_fence_after();
+      tmem_ld128_sync(tS, s);
       tc_fence_before();
-      mbar_arrive(bar_sfree);  // S_t(j) is in registers: S_t may be overwritten
+      mbar_arrive(bar_sfree(t));  // S_t(j) is in registers: S_t may be overwritten
 
       float alpha = 1.f;
       bool resc = false;    // warp-uniform: O_t is multiplied by alpha before PV(j)
-      bool exact = false;   // warp-uniform: the tile maximum was taken before the exponentials
       float2 acc[4];
       const float2 c2 = make_float2(c, c);
       float2 nm2 = make_float2(0.f, 0.f);
@@ -327,88 +313,87 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P_t
-      if (act) {
-        const int k0 = j * 128;
-        const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
-        if (edge) {
-          const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
+      const int k0 = j * 128;
+      const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
+      if (edge) {
+        const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (i >= lim) s[i] = -INFINITY;
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) s[i] = -INFINITY;
+      }
+      // Until a row has a finite running maximum its first tile takes the
+      // maximum before exponentiating; later tiles exponentiate against the
+      // running maximum and check the result afterwards (below).
+      const bool exact = __any_sync(0xffffffffu, m_run == -INFINITY);
+      if (exact) {
+        const float m_cand = fmaxf(m_run, row_max128(s) * c);
+        resc = __any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2);
+        if (resc) {
+          alpha = ex2_approx(m_run - ((m_cand == -INFINITY) ? 0.f : m_cand));
+          m_run = m_cand;
         }
-        // Until a row has a finite running maximum its first tile takes the
-        // maximum before exponentiating; later tiles exponentiate against the
-        // running maximum and check the result afterwards (below).
-        exact = __any_sync(0xffffffffu, m_run == -INFINITY);
-        if (exact) {
-          const float m_cand = fmaxf(m_run, row_max128(s) * c);
-          resc = __any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2);
-          if (resc) {
-            alpha = ex2_approx(m_run - ((m_cand == -INFINITY) ? 0.f : m_cand));
-            m_run = m_cand;
-          }
-        }
+      }
+      {
         const float m_safe = (m_run == -INFINITY) ? 0.f : m_run;
         nm2 = make_float2(-m_safe, -m_safe);
-#pragma unroll
-        for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
-        exp_block(0, pk[0]);
-        exp_block(1, pk[1]);
       }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+      exp_block(0, pk[0]);
+      exp_block(1, pk[1]);
+      if (t == 0 && j == 0) mbar_arrive(bar_go);
 
-      // PV(j-1) has completed: O_t is stable and P_t is free
+      // PV_t(j-1) has completed: O_t is stable and P_t is free
       if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv(t), (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
         if (!ok) break;
       }
-      if (act) {
-        tc_fence_after();
-        if (resc && j > 0) rescale_o();
-        tmem_st16(tP, pk[0]);
-        tmem_st16(tP + 16, pk[1]);
-        // keys 64-127: computed and stored now that P_t is free
+      tc_fence_after();
+      if (resc && j > 0) rescale_o();
+      tmem_st16(tP, pk[0]);
+      tmem_st16(tP + 16, pk[1]);
+      // keys 64-127: computed and stored now that P_t is free
 #pragma unroll
-        for (int cb = 2; cb < 4; ++cb) {
-          uint32_t w[16];
-          exp_block(cb, w);
-          tmem_st16(tP + 16 * cb, w);
-        }
-        float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-        if (!exact) {
-          // Every weight 2^(c s - m_run) is at most the tile's row sum, so a sum
-          // up to 2^kRescaleLog2 means the maximum grew by at most kRescaleLog2
-          // and the weights stand (the lazy rescale rule).  Otherwise take the
-          // maximum, and where it grew further, rescale and recompute the tile.
-          const bool check = !(a03.x + a03.y <= kRescaleBound);
-          if (__any_sync(0xffffffffu, check)) {
-            const float m_cand = fmaxf(m_run, row_max128(s) * c);
-            if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2)) {
-              alpha = ex2_approx(m_run - m_cand);
-              m_run = m_cand;
-              nm2 = make_float2(-m_cand, -m_cand);
+      for (int cb = 2; cb < 4; ++cb) {
+        uint32_t w[16];
+        exp_block(cb, w);
+        tmem_st16(tP + 16 * cb, w);
+      }
+      float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+      if (!exact) {
+        // Every weight 2^(c s - m_run) is at most the tile's row sum, so a sum
+        // up to 2^kRescaleLog2 means the maximum grew by at most kRescaleLog2
+        // and the weights stand (the lazy rescale rule).  Otherwise take the
+        // maximum, and where it grew further, rescale and recompute the tile.
+        const bool check = !(a03.x + a03.y <= kRescaleBound);
+        if (__any_sync(0xffffffffu, check)) {
+          const float m_cand = fmaxf(m_run, row_max128(s) * c);
+          if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2)) {
+            alpha = ex2_approx(m_run - m_cand);
+            m_run = m_cand;
+            nm2 = make_float2(-m_cand, -m_cand);
 #pragma unroll
-              for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+            for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
 #pragma unroll
-              for (int cb = 0; cb < 4; ++cb) {
-                uint32_t w[16];
-                exp_block(cb, w);
-                tmem_st16(tP + 16 * cb, w);
-              }
-              a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-              if (j > 0) rescale_o();
+            for (int cb = 0; cb < 4; ++cb) {
+              uint32_t w[16];
+              exp_block(cb, w);
+              tmem_st16(tP + 16 * cb, w);
             }
+            a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+            if (j > 0) rescale_o();
           }
         }
-        l_run = l_run * alpha + (a03.x + a03.y);
-        tmem_st_wait();
       }
+      l_run = l_run * alpha + (a03.x + a03.y);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(bar_p(t));
     }
 
     // epilogue: wait for the last PV, then O / l -> bf16, LSE
     if (ok && n > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (nkv - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_pv(t), (n - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
     if (ok && n > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
