@@ -271,11 +271,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
+    // first key tile with masked keys (past Lk, or above the causal diagonal)
+    const int j_edge = min(p.Lk / 128, p.causal ? qt / 128 : (1 << 30));
 
     // group 1 starts once group 0 has its first half tile of weights
     if (t == 1 && n > 0)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_go, 0, abort_flag, p.err, kSiteSoftmaxGo));
 
+#pragma unroll 2
     for (int j = 0; j < n && ok; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_s(t), j & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
@@ -314,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P_t
       const int k0 = j * 128;
-      const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
+      const bool edge = j >= j_edge;
       if (edge) {
         const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
 #pragma unroll
