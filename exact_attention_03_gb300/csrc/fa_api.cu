@@ -52,6 +52,32 @@ EncodeTiledFn encode_fn() {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The library's stream-ordered workspace pool on device `dev`.  Its release
+// threshold is the maximum, so memory freed at the end of a call stays in the
+// pool for the next one instead of being unmapped at the next synchronisation.
+cudaMemPool_t workspace_pool(int dev) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pools[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = UINT64_MAX;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return nullptr;
+    }
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
 __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
   __shared__ alignas(8) unsigned long long bar;
   __shared__ int abort_flag;
@@ -66,6 +92,18 @@ __global__ void wait_selftest_kernel(int* err, unsigned long long limit_ns) {
 }
 
 }  // namespace
+
+int workspace_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaMemPool_t pool = workspace_pool(dev);
+  if (pool == nullptr) return FA_ERR_CUDA;
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int workspace_free(void* ptr, cudaStream_t stream) {
+  return cudaFreeAsync(ptr, stream) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
 
 int make_tensor_map_bf16(CUtensorMap* map, const void* ptr, int BH, int L, int D) {
   EncodeTiledFn enc = encode_fn();
@@ -154,10 +192,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     const int n_split = fa_decode_num_splits(int(BH), Lk, sms);
     const size_t ws_bytes = size_t(n_split) * size_t(BH) * size_t(D + 2) * sizeof(float);
     void* ws = nullptr;
-    if (cudaMallocAsync(&ws, ws_bytes, s) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::workspace_alloc(&ws, ws_bytes, s) != FA_OK) return FA_ERR_CUDA;
     const int st = fa::launch_decode(q, k, v, o, lse, int(BH), Lk, D, scale, n_split,
                                      static_cast<float*>(ws), s);
-    const bool freed = cudaFreeAsync(ws, s) == cudaSuccess;
+    const bool freed = fa::workspace_free(ws, s) == FA_OK;
     if (st != FA_OK) return st;
     return freed ? FA_OK : FA_ERR_CUDA;
   }

@@ -39,6 +39,11 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
 
 int num_sms_of_current_device(int* num_sms);
 
+// Workspace memory, stream-ordered on `stream`, from the library's pool of the
+// current device (kept between calls).  Return FA_OK or FA_ERR_CUDA.
+int workspace_alloc(void** ptr, size_t bytes, cudaStream_t stream);
+int workspace_free(void* ptr, cudaStream_t stream);
+
 // TMA tensor map over a [BH, L, D] bf16 tensor, viewed as {64, L, D/64, BH}: one
 // box is a 128-row tile of one head (D/64 swizzled blocks of 128 rows x 128 B),
 // rows past L read as zeros.  Returns 0 or FA_ERR_CUDA.

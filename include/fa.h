@@ -58,8 +58,11 @@ typedef enum {
  * Ownership: the caller owns every buffer; the library keeps no pointer after
  * the call returns.  The single-query path (Lq == 1, non-causal) splits the
  * keys over many thread blocks and needs a workspace of
- * n_split * B * H * (D + 2) * 4 bytes, which it allocates and frees
- * stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ * n_split * B * H * (D + 2) * 4 bytes, allocated and freed stream-ordered on
+ * `stream` from a memory pool the library creates per device
+ * (cudaMemPoolCreate; the pool keeps freed memory for later calls, so that a
+ * call after a synchronisation does not map new memory, and lives until the
+ * process ends).
  *
  * Errors: arguments are checked on the host before any CUDA call, and a bad
  * argument returns FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_MISALIGNED
