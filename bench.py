@@ -300,6 +300,36 @@ def per_config(args, fa, flush, dev, peaks, check):
         out[name] = entry
         del q, k, v, o, lse
         torch.cuda.empty_cache()
+    out.update(per_config_paged(fa, flush, dev, peaks, check))
+    return out
+
+
+def per_config_paged(fa, flush, dev, peaks, check):
+    """Single-query attention against the paged cache (fa_fwd_decode_paged):
+    GB/s over the algorithmic bytes (every cached K and V row of every
+    sequence once, q once, O and LSE once)."""
+    import torch
+    from exact_attention_03_gb300.inputs import PAGED_WORKLOADS, make_paged_inputs
+    out = {}
+    for name, reps in (("decode_paged_128k_d128", 5),):
+        w = PAGED_WORKLOADS[name]
+        q, kc, vc, bt, lens = make_paged_inputs(w, dev)
+        o = torch.empty((w.B, w.H, w.D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((w.B, w.H), dtype=torch.float32, device=dev)
+        call = lambda: fa.decode_paged(q, kc, vc, bt, lens, out=o, lse=lse)
+        _time_launches([call], flush, 2)
+        ts = _time_launches([call], flush, reps)
+        check()
+        ms = statistics.median(ts)
+        total = int(lens.sum().item())
+        nbytes = total * w.H * w.D * 2 * 2 + w.B * w.H * (w.D * 2 * 2 + 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"B": w.B, "H": w.H, "D": w.D, "page_size": w.page_size,
+                     "max_len": w.max_len, "cached_positions": total, "ms": round(ms, 5),
+                     "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                     "launches": 2, "algorithmic_bytes": nbytes}
+        del q, kc, vc, bt, lens, o, lse
+        torch.cuda.empty_cache()
     return out
 
 

@@ -19,7 +19,7 @@ from typing import Optional, Tuple
 __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
-           "forward", "forward_host", "decode_noalloc", "EXPORTED_SYMBOLS"]
+           "forward", "forward_host", "decode_noalloc", "decode_paged", "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -48,6 +48,11 @@ _SIGS = {
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_float, ctypes.c_void_p]),
     "fa_decode_noalloc_max_floats": (ctypes.c_int, []),
+    "fa_fwd_decode_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_float, ctypes.c_void_p]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -174,6 +179,52 @@ def decode_noalloc(q, k, v, scale: Optional[float] = None, out=None, lse=None, s
                                       _stream_handle(stream))
     if st != FA_OK:
         raise FlashAttentionError(st, "fa_fwd_decode_noalloc")
+    return out, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: Optional[float] = None,
+                 out=None, lse=None, stream=None):
+    """Single-query attention against a paged cache through fa_fwd_decode_paged.
+
+    q: bf16 [B, H, D] or [B, H, 1, D]; k_cache, v_cache: bf16 [num_pages,
+    page_size, H, D]; block_table: int32 [B, max_pages_per_seq]; seq_lens:
+    int32 [B]; all CUDA tensors.  Returns O (bf16, shaped like q) and LSE
+    (fp32 [B, H])."""
+    import torch
+
+    if q.dim() == 4:
+        if q.shape[2] != 1:
+            raise ValueError("decode_paged takes one query row per head")
+        B, H, _, D = q.shape
+    elif q.dim() == 3:
+        B, H, D = q.shape
+    else:
+        raise ValueError("q must be [B, H, D] or [B, H, 1, D]")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache, v_cache must both be [num_pages, page_size, H, D]")
+    num_pages, page_size, Hc, Dc = k_cache.shape
+    if (Hc, Dc) != (H, D):
+        raise ValueError(f"cache heads/dim {Hc, Dc} do not match q {H, D}")
+    if block_table.dim() != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages_per_seq] and seq_lens [B]")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+    for name, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA int32 tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    st = load().fa_fwd_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                    block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), B, H, D, num_pages, page_size,
+                                    block_table.shape[1], float(scale), _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_fwd_decode_paged")
     return out, lse
 
 

@@ -212,7 +212,54 @@ int fa_last_device_error(void* stream, int* site) {
     if (cudaMemcpyToSymbol(fa::g_device_error, zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
   if (site != nullptr) *site = h[1];
-  return h[0] == 0 ? FA_OK : FA_ERR_TIMEOUT;
+  return h[0];  // FA_OK, FA_ERR_TIMEOUT, or FA_ERR_INVALID_ARG (a page id out of range)
+}
+
+int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                        const int* block_table, const int* seq_lens, void* o, float* lse, int B,
+                        int H, int D, int num_pages, int page_size, int max_pages_per_seq,
+                        float scale, void* stream) {
+  // ---- host-side checks, before any CUDA call
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || block_table == nullptr ||
+      seq_lens == nullptr || o == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || D <= 0 || num_pages <= 0 || page_size <= 0 || max_pages_per_seq <= 0)
+    return FA_ERR_INVALID_ARG;
+  if ((page_size & (page_size - 1)) != 0 || page_size > 65536) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  const long long max_len = (long long)max_pages_per_seq * page_size;
+  if (BH > 0x7fffffffLL || max_len > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (!fa::aligned(q, 16) || !fa::aligned(k_cache, 16) || !fa::aligned(v_cache, 16) ||
+      !fa::aligned(o, 16))
+    return FA_ERR_MISALIGNED;
+  if (!fa::aligned(block_table, 4) || !fa::aligned(seq_lens, 4) ||
+      (lse != nullptr && !fa::aligned(lse, 4)))
+    return FA_ERR_MISALIGNED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int* err = fa::error_word_ptr(dev);
+  if (err == nullptr) return FA_ERR_CUDA;
+  int sms = 0;
+  if (fa::num_sms_of_current_device(&sms) != FA_OK) return FA_ERR_CUDA;
+  // splits sized for the longest sequence the page table can address; a split
+  // stages at most 2048 page ids, which short pages can require more splits for
+  long long n_split = fa_decode_num_splits(int(BH), int(max_len), sms);
+  const long long per_split = 2046LL * page_size;
+  if (n_split < (max_len + per_split - 1) / per_split) n_split = (max_len + per_split - 1) / per_split;
+  const size_t ws_bytes = size_t(n_split) * size_t(BH) * size_t(D + 2) * sizeof(float);
+  void* ws = nullptr;
+  if (fa::workspace_alloc(&ws, ws_bytes, s) != FA_OK) return FA_ERR_CUDA;
+  const int st = fa::launch_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, H,
+                                         D, num_pages, page_size, max_pages_per_seq, scale,
+                                         int(n_split), static_cast<float*>(ws), err, s);
+  const bool freed = fa::workspace_free(ws, s) == FA_OK;
+  if (st == -2) return FA_ERR_UNSUPPORTED;
+  if (st != 0) return FA_ERR_CUDA;
+  return freed ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_wait_selftest(int limit_us, void* stream) {

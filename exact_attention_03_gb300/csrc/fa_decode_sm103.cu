@@ -19,6 +19,15 @@
 //     with the same rescale identity (M = max m_s, l = sum l_s 2^(m_s - M),
 //     O = sum O_s 2^(m_s - M) / l) and writes O (bf16) and LSE (fp32).
 // Exponentials are base 2: x = q.k * scale * log2(e).
+//
+// The same kernels serve a paged key/value cache (fa_fwd_decode_paged): keys
+// and values of sequence b live in pages of page_size positions, [num_pages,
+// page_size, H, D], listed in order by row b of a page table; sequence b has
+// seq_lens[b] positions.  A split then covers positions [split*chunk, ...) of
+// its sequence, looks the pages up through the table (staged in shared memory,
+// every page id bounds-checked), and splits past the sequence's end leave an
+// empty partial (m = -inf, l = 0) that the combine weighs with zero.
+#include "fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -43,7 +52,13 @@ struct DecParams {
   float* part_ml;  // [n_split][BH][2]  (m in log2 units, l)
   int BH, Lk, n_split, chunk;
   float scale_log2;
+  // paged cache only
+  const int* block_table;  // [B][max_pages]
+  const int* seq_lens;     // [B]
+  int* err;                // device error word: a page id out of range
+  int H, max_pages, num_pages, page_shift;
 };
+constexpr int kMaxPagesPerSplit = 2048;   // page-table entries one split stages
 
 __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
   uint4 r;
@@ -55,13 +70,14 @@ __device__ __forceinline__ uint4 ld_stream16(const void* ptr) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecParams p) {
   constexpr int G = D / 8;             // lanes per key
   constexpr int GPW = 32 / G;          // key groups per warp
   constexpr int NG = kDecWarps * GPW;  // key groups per CTA
   __shared__ float sm_m[NG], sm_l[NG];
   __shared__ float sm_acc[NG][D];
+  __shared__ int sm_page[PAGED ? kMaxPagesPerSplit : 1];
 
   const int split = int(blockIdx.x) % p.n_split;
   const int bh = int(blockIdx.x) / p.n_split;
@@ -81,11 +97,36 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecP
     }
   }
 
-  const size_t head = size_t(bh) * size_t(p.Lk) * D;
-  const __nv_bfloat16* kp = p.k + head + 8 * li;
-  const __nv_bfloat16* vp = p.v + head + 8 * li;
   const int kbeg = split * p.chunk;
-  const int kend = min(kbeg + p.chunk, p.Lk);
+  int kend;
+  const __nv_bfloat16* kp;
+  const __nv_bfloat16* vp;
+  if constexpr (PAGED) {
+    // this sequence's length, clamped to what its page-table row can address
+    const int b = bh / p.H;
+    const int len = min(max(p.seq_lens[b], 0), p.max_pages << p.page_shift);
+    kend = min(kbeg + p.chunk, len);
+    // page ids of positions [kbeg, kend), checked against the cache size
+    const int pg0 = kbeg >> p.page_shift;
+    const int npg = kend > kbeg ? ((kend - 1) >> p.page_shift) - pg0 + 1 : 0;
+    for (int i = threadIdx.x; i < npg; i += kDecThreads) {
+      int pg = p.block_table[size_t(b) * p.max_pages + pg0 + i];
+      if (pg < 0 || pg >= p.num_pages) {  // record it; the page's keys stay unread
+        if (atomicCAS(p.err, 0, FA_ERR_INVALID_ARG) == 0) atomicExch(p.err + 1, kSitePageTable);
+        pg = -1;
+      }
+      sm_page[i] = pg;
+    }
+    __syncthreads();
+    const int h = bh - b * p.H;
+    kp = p.k + size_t(h) * D + 8 * li;   // + (page * page_size + offset) * H * D
+    vp = p.v + size_t(h) * D + 8 * li;
+  } else {
+    const size_t head = size_t(bh) * size_t(p.Lk) * D;
+    kp = p.k + head + 8 * li;
+    vp = p.v + head + 8 * li;
+    kend = min(kbeg + p.chunk, p.Lk);
+  }
 
   float m = -INFINITY, l = 0.f, acc[8];
 #pragma unroll
@@ -99,9 +140,18 @@ __global__ void __launch_bounds__(kDecThreads) fa_decode_split_kernel(const DecP
     for (int u = 0; u < kUnroll; ++u) {
       const int key = base + u * NG + gi;
       valid[u] = key < kend;
+      size_t row = size_t(key);
+      if constexpr (PAGED) {
+        if (valid[u]) {
+          const int pg = sm_page[(key >> p.page_shift) - (kbeg >> p.page_shift)];
+          valid[u] = pg >= 0;
+          row = (size_t(pg) << p.page_shift) + (key & ((1 << p.page_shift) - 1));
+          row *= size_t(p.H);
+        }
+      }
       if (valid[u]) {
-        kr[u] = ld_stream16(kp + size_t(key) * D);
-        vr[u] = ld_stream16(vp + size_t(key) * D);
+        kr[u] = ld_stream16(kp + row * D);
+        vr[u] = ld_stream16(vp + row * D);
       } else {
         kr[u] = make_uint4(0, 0, 0, 0);
         vr[u] = make_uint4(0, 0, 0, 0);
@@ -226,17 +276,19 @@ __global__ void __launch_bounds__(kCombThreads) fa_decode_combine_kernel(const D
       o0 += red_acc[w][d];
       o1 += red_acc[w][d + 1];
     }
-    const float inv = 1.f / L_tot;
+    // an empty row (a paged sequence of length 0) has L_tot = 0: O = 0, LSE = -inf
+    const float inv = L_tot > 0.f ? 1.f / L_tot : 0.f;
     *reinterpret_cast<uint32_t*>(p.o + size_t(bh) * D + d) = pack_bf16x2(o0 * inv, o1 * inv);
-    if (threadIdx.x == 0 && p.lse != nullptr) p.lse[bh] = (M + __log2f(L_tot)) * kLn2;
+    if (threadIdx.x == 0 && p.lse != nullptr)
+      p.lse[bh] = L_tot > 0.f ? (M + __log2f(L_tot)) * kLn2 : -INFINITY;
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 int launch(const DecParams& p, cudaStream_t stream) {
   const long long nblk = (long long)p.BH * p.n_split;
   if (nblk > 0x7fffffffLL) return -2;
-  fa_decode_split_kernel<D><<<dim3(unsigned(nblk)), dim3(kDecThreads), 0, stream>>>(p);
+  fa_decode_split_kernel<D, PAGED><<<dim3(unsigned(nblk)), dim3(kDecThreads), 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return -4;
   fa_decode_combine_kernel<D><<<dim3(unsigned(p.BH)), dim3(kCombThreads), 0, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
@@ -259,8 +311,48 @@ int launch_decode(const void* q, const void* k, const void* v, void* o, float* l
   p.part_o = workspace;
   p.part_ml = workspace + size_t(n_split) * BH * D;
   p.scale_log2 = scale * 1.44269504088896340736f;
-  if (D == 64) return launch<64>(p, stream);
-  if (D == 128) return launch<128>(p, stream);
+  p.block_table = nullptr;
+  p.seq_lens = nullptr;
+  p.err = nullptr;
+  p.H = 1;
+  p.max_pages = 0;
+  p.num_pages = 0;
+  p.page_shift = 0;
+  if (D == 64) return launch<64, false>(p, stream);
+  if (D == 128) return launch<128, false>(p, stream);
+  return -2;
+}
+
+int launch_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                        const int* block_table, const int* seq_lens, void* o, float* lse, int B,
+                        int H, int D, int num_pages, int page_size, int max_pages, float scale,
+                        int n_split, float* workspace, int* err, cudaStream_t stream) {
+  DecParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k_cache);
+  p.v = static_cast<const __nv_bfloat16*>(v_cache);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.BH = B * H;
+  const long long max_len = (long long)max_pages * page_size;
+  p.Lk = int(max_len);
+  p.n_split = n_split;
+  p.chunk = int((max_len + n_split - 1) / n_split);
+  if ((p.chunk + page_size - 1) / page_size + 1 > kMaxPagesPerSplit) return -2;
+  p.part_o = workspace;
+  p.part_ml = workspace + size_t(n_split) * p.BH * D;
+  p.scale_log2 = scale * 1.44269504088896340736f;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.err = err;
+  p.H = H;
+  p.max_pages = max_pages;
+  p.num_pages = num_pages;
+  int shift = 0;
+  while ((1 << shift) < page_size) ++shift;
+  p.page_shift = shift;
+  if (D == 64) return launch<64, true>(p, stream);
+  if (D == 128) return launch<128, true>(p, stream);
   return -2;
 }
 

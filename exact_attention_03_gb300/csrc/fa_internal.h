@@ -20,6 +20,7 @@ enum WaitSite : int {
   kSiteSelftest = 8,
   kSiteMmaS = 9,
   kSiteSoftmaxGo = 10,
+  kSitePageTable = 11,  // not a wait: a page id outside the paged cache (FA_ERR_INVALID_ARG)
 };
 
 // Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
@@ -36,6 +37,15 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
 // `workspace` must hold n_split * B * H * (D + 2) floats.
 int launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int BH,
                   int Lk, int D, float scale, int n_split, float* workspace, cudaStream_t stream);
+
+// Single-query attention over a paged cache (fa_fwd_decode_paged): arguments
+// already validated; `workspace` holds n_split * B * H * (D + 2) floats; `err`
+// is the device error word.  Returns 0, -2 (a split would need more than 2048
+// page-table entries) or -4.
+int launch_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                        const int* block_table, const int* seq_lens, void* o, float* lse, int B,
+                        int H, int D, int num_pages, int page_size, int max_pages, float scale,
+                        int n_split, float* workspace, int* err, cudaStream_t stream);
 
 int num_sms_of_current_device(int* num_sms);
 

@@ -28,6 +28,17 @@ Recipe (the same on any device, deterministic for a device):
     randperm(Lq)[:n-2]; rows 0 and Lq-1 are always added.
 The CPU and CUDA torch generators give different streams, so a test makes its
 inputs once and hands the same bf16 tensors to both sides.
+
+Paged single-query decode (PagedWorkload, make_paged_inputs): B sequences, H
+heads, pages of page_size positions, lengths up to max_len.
+  * lengths: a generator seeded (seed << 20) | (1 << 17) draws randint in
+    [1, max_len] per sequence (or `lengths` gives them);
+  * pages: sequence b needs ceil(len_b / page_size) pages; all pages are
+    numbered by a randperm from a generator seeded (seed << 20) | (1 << 16)
+    and handed out in sequence order; unused page-table entries are -1;
+  * q [B, H, D], then the caches [num_pages, page_size, H, D] (k, then v):
+    randn in fp32 from generators seeded (seed << 20) | t (t = 0, 1, 2),
+    cast to bf16.
 """
 from __future__ import annotations
 
@@ -38,7 +49,8 @@ from typing import Optional
 import torch
 
 __all__ = ["Workload", "WORKLOADS", "SWEEP_LENGTHS", "sweep", "make_inputs",
-           "sample_rows", "outlier_rows"]
+           "sample_rows", "outlier_rows", "PagedWorkload", "PAGED_WORKLOADS",
+           "make_paged_inputs"]
 
 
 @dataclass(frozen=True)
@@ -152,3 +164,66 @@ def sample_rows(w: Workload, n: Optional[int] = None):
         r = torch.cat([torch.tensor([0, w.Lq - 1]), inner])
         rows.append(torch.sort(r).values)
     return rows
+
+
+@dataclass(frozen=True)
+class PagedWorkload:
+    name: str
+    B: int
+    H: int
+    D: int
+    page_size: int
+    max_len: int
+    seed: int
+    lengths: Optional[tuple] = None   # fixed lengths instead of drawn ones
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def max_pages(self) -> int:
+        return (self.max_len + self.page_size - 1) // self.page_size
+
+
+PAGED_WORKLOADS = {
+    # 16 sequences of up to 128K cached positions, 16-position pages
+    "decode_paged_128k_d128": PagedWorkload("decode_paged_128k_d128", 16, 32, 128, 16, 131072, 5),
+}
+
+
+def paged_lengths(w: PagedWorkload) -> torch.Tensor:
+    if w.lengths is not None:
+        return torch.tensor(w.lengths, dtype=torch.int32)
+    g = _gen("cpu", (w.seed << 20) | (1 << 17))
+    return torch.randint(1, w.max_len + 1, (w.B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def make_paged_inputs(w: PagedWorkload, device="cpu"):
+    """q [B,H,D], k_cache, v_cache [num_pages, page_size, H, D] (bf16),
+    block_table [B, max_pages] and seq_lens [B] (int32), all on `device`."""
+    device = torch.device(device)
+    lens = paged_lengths(w)
+    need = [min(w.max_pages, (max(int(L), 0) + w.page_size - 1) // w.page_size) for L in lens.tolist()]
+    num_pages = max(1, sum(need))
+    g = _gen("cpu", (w.seed << 20) | (1 << 16))
+    order = torch.randperm(num_pages, generator=g)
+    table = torch.full((w.B, w.max_pages), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(need):
+        table[b, :n] = order[at:at + n].to(torch.int32)
+        at += n
+    out = []
+    for t, shape in enumerate(((w.B, w.H, w.D), (num_pages, w.page_size, w.H, w.D),
+                               (num_pages, w.page_size, w.H, w.D))):
+        x = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        gg = _gen(device, (w.seed << 20) | t)
+        flat = x.view(-1, shape[-1])
+        step = 1 << 20   # rows per draw, bounds the fp32 temporary
+        for r0 in range(0, flat.shape[0], step):
+            r1 = min(flat.shape[0], r0 + step)
+            flat[r0:r1].copy_(torch.randn((r1 - r0, shape[-1]), generator=gg, device=device,
+                                          dtype=torch.float32))
+        out.append(x)
+    q, kc, vc = out
+    return q, kc, vc, table.to(device), lens.to(device)

@@ -84,10 +84,12 @@ const char* fa_strerror(int status);
 
 /*
  * fa_last_device_error - synchronises `stream`, then reads and clears the
- * library's device error word on the current device.  Returns FA_OK when no
- * device-side wait has given up since the last call, else FA_ERR_TIMEOUT
- * (FA_ERR_CUDA if the synchronisation itself fails).  If `site` is not NULL it
- * receives an identifier of the wait that gave up (0 when none).
+ * library's device error word on the current device.  Returns FA_OK when
+ * nothing was recorded since the last call, FA_ERR_TIMEOUT when a device-side
+ * wait gave up, FA_ERR_INVALID_ARG when fa_fwd_decode_paged met a page id
+ * outside its cache (FA_ERR_CUDA if the synchronisation itself fails); the
+ * first event recorded wins.  If `site` is not NULL it receives an identifier
+ * of where it happened (0 when none).
  */
 int fa_last_device_error(void* stream, int* site);
 
@@ -140,10 +142,46 @@ int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, 
 /* fa_decode_noalloc_max_floats - size, in floats, of fa_fwd_decode_noalloc's array. */
 int fa_decode_noalloc_max_floats(void);
 
+/*
+ * fa_fwd_decode_paged - single-query attention (one query row per head,
+ * non-causal) against a paged key/value cache with a length per sequence:
+ * the decode step of generation over a cache that grows page by page.  The
+ * lecture leaves the cache's layout to its next part; this one is the plainest
+ * paged form.  For every sequence b and head h it computes what fa_fwd
+ * computes for q[b, h] against the seq_lens[b] cached positions of that
+ * sequence, in order:
+ *   position p of sequence b sits in page block_table[b * max_pages_per_seq +
+ *   p / page_size], row p % page_size of that page.
+ *
+ * q        : device, bf16, [B, H, D] (= [B, H, 1, D]), contiguous.
+ * k_cache, v_cache : device, bf16, [num_pages, page_size, H, D], contiguous
+ *            (within a page: position-major, then head, then D).
+ * block_table : device, int32, [B, max_pages_per_seq]; entries past a
+ *            sequence's last page are not read.  An entry that is read and is
+ *            outside [0, num_pages) is recorded in the device error word
+ *            (FA_ERR_INVALID_ARG, see fa_last_device_error) and that page's
+ *            keys are left out; nothing is read out of bounds.
+ * seq_lens : device, int32, [B]; values are clamped to
+ *            [0, max_pages_per_seq * page_size].  A sequence of length 0 gets
+ *            O = 0 and LSE = -inf.
+ * o, lse   : bf16 [B, H, D] and fp32 [B, H] (lse may be NULL), written.
+ * page_size: a power of two, 1 .. 65536.  D in {64, 128}; finite scale > 0.
+ *
+ * Workspace: n_split * B * H * (D + 2) * 4 bytes from the library's pool
+ * (see fa_fwd), n_split as fa_decode_num_splits for Lk = max_pages_per_seq *
+ * page_size, raised where one split would span more than 2046 pages.
+ * Errors and asynchrony as for fa_fwd (q, k_cache, v_cache, o 16-byte aligned;
+ * block_table, seq_lens, lse 4-byte aligned).
+ */
+int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,
+                        const int* block_table, const int* seq_lens, void* o, float* lse,
+                        int B, int H, int D, int num_pages, int page_size,
+                        int max_pages_per_seq, float scale, void* stream);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 0)
+#define FA_ABI_VERSION ((1 << 16) | 1)
 
 #ifdef __cplusplus
 }

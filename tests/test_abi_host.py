@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
-              "fa_wait_selftest", "fa_abi_version"):
+              "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged"):
         assert n in names
 
 
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16)
+    assert lib.fa_abi_version() == (1 << 16) | 1
 
 
 def test_strerror_covers_every_status(lib):
@@ -133,3 +133,43 @@ def test_binding_rejects_bad_tensors(lib):
         fa.forward(q, q, q)  # CPU tensors are refused; no silent fallback
     with pytest.raises(ValueError):
         fa.forward(q[0], q, q)
+
+
+def call_paged(**kw):
+    args = dict(q=A, kc=A, vc=A, bt=A, lens=A, o=A, lse=A, B=2, H=4, D=128, num_pages=64,
+                page_size=16, max_pages=8, scale=0.1)
+    args.update(kw)
+    return fa.load().fa_fwd_decode_paged(args["q"], args["kc"], args["vc"], args["bt"], args["lens"],
+                                         args["o"], args["lse"], args["B"], args["H"], args["D"],
+                                         args["num_pages"], args["page_size"], args["max_pages"],
+                                         args["scale"], None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(kc=None), fa.FA_ERR_INVALID_ARG),
+    (dict(vc=None), fa.FA_ERR_INVALID_ARG),
+    (dict(bt=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lens=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=0), fa.FA_ERR_INVALID_ARG),
+    (dict(num_pages=0), fa.FA_ERR_INVALID_ARG),
+    (dict(page_size=0), fa.FA_ERR_INVALID_ARG),
+    (dict(page_size=24), fa.FA_ERR_INVALID_ARG),
+    (dict(page_size=1 << 17), fa.FA_ERR_INVALID_ARG),
+    (dict(max_pages=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(page_size=1 << 16, max_pages=1 << 16), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(kc=A + 4), fa.FA_ERR_MISALIGNED),
+    (dict(vc=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(bt=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lens=A + 1), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_paged_bad_arguments_rejected_on_host(lib, kw, expect):
+    assert call_paged(**kw) == expect
