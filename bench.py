@@ -301,6 +301,33 @@ def per_config(args, fa, flush, dev, peaks, check):
         del q, k, v, o, lse
         torch.cuda.empty_cache()
     out.update(per_config_paged(fa, flush, dev, peaks, check))
+    out.update(per_config_softmax(fa, flush, dev, peaks, check))
+    return out
+
+
+def per_config_softmax(fa, flush, dev, peaks, check):
+    """The two-read row softmax (fa_softmax_rows) on a 1 GiB fp32 matrix: GB/s
+    over the bytes every softmax must move (x read once, y written once); the
+    second read of a row comes back from L2 right after the first."""
+    import torch
+    out = {}
+    rows, cols = 32768, 8192
+    g = torch.Generator(device=dev).manual_seed(10)
+    x = torch.randn(rows, cols, generator=g, device=dev) * 4
+    y = torch.empty_like(x)
+    lse = torch.empty(rows, dtype=torch.float32, device=dev)
+    call = lambda: fa.softmax_rows(x, out=y, lse=lse)
+    _time_launches([call], flush, 3)
+    ts = _time_launches([call], flush, 20)
+    check()
+    ms = statistics.median(ts)
+    nbytes = rows * cols * 4 * 2 + rows * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["softmax_rows_32k_x_8k"] = {"rows": rows, "cols": cols, "ms": round(ms, 5),
+                                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                                    "launches": 1, "algorithmic_bytes": nbytes}
+    del x, y, lse
+    torch.cuda.empty_cache()
     return out
 
 

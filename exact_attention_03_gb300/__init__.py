@@ -19,7 +19,8 @@ from typing import Optional, Tuple
 __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED",
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
-           "forward", "forward_host", "decode_noalloc", "decode_paged", "EXPORTED_SYMBOLS"]
+           "forward", "forward_host", "decode_noalloc", "decode_paged", "softmax_rows",
+           "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -53,6 +54,8 @@ _SIGS = {
                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_float, ctypes.c_void_p]),
+    "fa_softmax_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -225,6 +228,28 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: Optional[flo
                                     block_table.shape[1], float(scale), _stream_handle(stream))
     if st != FA_OK:
         raise FlashAttentionError(st, "fa_fwd_decode_paged")
+    return out, lse
+
+
+def softmax_rows(x, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Row softmax of a CUDA fp32 tensor (last dimension = columns) through
+    fa_softmax_rows.  Returns (y, lse) with y shaped like x and lse like
+    x.shape[:-1] (None when return_lse is false)."""
+    import torch
+
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous() or x.dim() < 1:
+        raise ValueError("x must be a contiguous CUDA fp32 tensor")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols > 0 else 0
+    if out is None:
+        out = torch.empty_like(x)
+    if return_lse and lse is None:
+        lse = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    st = load().fa_softmax_rows(x.data_ptr(), out.data_ptr(),
+                                lse.data_ptr() if lse is not None else None, rows, cols,
+                                _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_softmax_rows")
     return out, lse
 
 

@@ -1,0 +1,172 @@
+// fa_softmax_sm103.cu - row softmax in two reads (fa_softmax_rows).
+//
+// "NTU Hung-yi Lee ML 2026 Guide: Faster Generation, Part 1: Flash Attention"
+// (quidproquo.cc), "Expand: why multiplying by exp(d1 - d2) fixes it": a row's
+// maximum and denominator can be found in one read, chunk by chunk, keeping a
+// running maximum d and a running sum s that is multiplied by exp(d_old -
+// d_new) whenever the maximum grows; a second read then writes the weights
+// exp(a_i - Amax) / S.  This file is that two-read softmax as an operation of
+// its own over the rows of a matrix:
+//
+//   read 1: every thread keeps (d, s) over the 4-element groups it reads
+//           (one rescale per group), then the pairs of a warp, and of the warps
+//           of a CTA, are merged with the same identity (d = max, s = s1
+//           exp(d1 - d) + s2 exp(d2 - d));
+//   read 2: y_i = exp(a_i - d) / s, written once.
+//
+// A row of up to kWarpCols columns is one warp's (8 rows per CTA); a longer row
+// is one CTA's (256 threads).  Exponentials are base 2: the running maximum is
+// kept as D = d log2 e (rounded once), every term as 2^(a log2 e - D) (one fused
+// multiply-add) and every rescale as 2^(D_old - D_new), so that all terms of a
+// row share one reference.  Rows are independent; the grid walks them in
+// strides.
+#include "fa.h"
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+#include <cstdint>
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarpCols = 2048;
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+// (D, s) after adding the values v[0..n): D = running maximum times log2 e,
+// s = sum of 2^(a log2 e - D); one rescale of s for the group
+__device__ __forceinline__ void online_group(float& D, float& s, const float* v, int n) {
+  float mx = v[0];
+  for (int i = 1; i < n; ++i) mx = fmaxf(mx, v[i]);
+  const float Dn = fmaxf(D, mx * kLog2e);
+  if (Dn == -INFINITY) return;  // every value so far is -inf
+  float add = 0.f;
+  for (int i = 0; i < n; ++i) add += ex2_approx(fmaf(v[i], kLog2e, -Dn));
+  s = s * ex2_approx(D - Dn) + add;
+  D = Dn;
+}
+
+// merge of two partial (D, s) pairs
+__device__ __forceinline__ void merge(float& D, float& s, float D2, float s2) {
+  const float Dn = fmaxf(D, D2);
+  if (Dn == -INFINITY) return;  // both empty
+  s = s * ex2_approx(D - Dn) + s2 * ex2_approx(D2 - Dn);
+  D = Dn;
+}
+
+// read 1 over this thread's share of a row: vector loads when the row is
+// 16-byte aligned, scalar loads otherwise
+__device__ __forceinline__ void scan(const float* row, int cols, int t, int nt, float& d, float& s) {
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    const int n4 = cols >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    for (int i = t; i < n4; i += nt) {
+      const float4 v4 = __ldg(r4 + i);
+      const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+      online_group(d, s, v, 4);
+    }
+    for (int i = (n4 << 2) + t; i < cols; i += nt) online_group(d, s, row + i, 1);
+  } else {
+    for (int i = t; i < cols; i += nt) {
+      const float v = __ldg(row + i);
+      online_group(d, s, &v, 1);
+    }
+  }
+}
+
+// read 2: y = 2^(a log2 e - D) / s (a row without any finite value gives 0)
+__device__ __forceinline__ void write_row(const float* row, float* out, int cols, int t, int nt,
+                                          float D, float s) {
+  const bool empty = !(s > 0.f);
+  const float inv = empty ? 0.f : 1.f / s;
+  const float ds = empty ? 0.f : D;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+    const int n4 = cols >> 2;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    float4* o4 = reinterpret_cast<float4*>(out);
+    for (int i = t; i < n4; i += nt) {
+      const float4 v = __ldg(r4 + i);
+      o4[i] = make_float4(ex2_approx(fmaf(v.x, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.y, kLog2e, -ds)) * inv,
+                          ex2_approx(fmaf(v.z, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.w, kLog2e, -ds)) * inv);
+    }
+    for (int i = (n4 << 2) + t; i < cols; i += nt) out[i] = ex2_approx(fmaf(row[i], kLog2e, -ds)) * inv;
+  } else {
+    for (int i = t; i < cols; i += nt) out[i] = ex2_approx(fmaf(__ldg(row + i), kLog2e, -ds)) * inv;
+  }
+}
+
+__device__ __forceinline__ void warp_merge(float& d, float& s) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float d2 = __shfl_xor_sync(0xffffffffu, d, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge(d, s, d2, s2);
+  }
+}
+
+// rows of up to kWarpCols columns: one warp per row
+__global__ void __launch_bounds__(kThreads) softmax_rows_warp(const float* x, float* y, float* lse,
+                                                              long long rows, int cols) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (kThreads / 32);
+  for (long long r = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
+    const float* row = x + r * cols;
+    float d = -INFINITY, s = 0.f;
+    scan(row, cols, lane, 32, d, s);
+    warp_merge(d, s);
+    write_row(row, y + r * cols, cols, lane, 32, d, s);
+    if (lse != nullptr && lane == 0) lse[r] = (s > 0.f) ? (d + __log2f(s)) * kLn2 : -INFINITY;
+  }
+}
+
+// longer rows: one CTA per row
+__global__ void __launch_bounds__(kThreads) softmax_rows_cta(const float* x, float* y, float* lse,
+                                                             long long rows, int cols) {
+  __shared__ float sd[kThreads / 32], ss[kThreads / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float* row = x + r * cols;
+    float d = -INFINITY, s = 0.f;
+    scan(row, cols, threadIdx.x, kThreads, d, s);
+    warp_merge(d, s);
+    if (lane == 0) {
+      sd[warp] = d;
+      ss[warp] = s;
+    }
+    __syncthreads();
+    d = sd[0];
+    s = ss[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) merge(d, s, sd[w], ss[w]);
+    write_row(row, y + r * cols, cols, threadIdx.x, kThreads, d, s);
+    if (lse != nullptr && threadIdx.x == 0) lse[r] = (s > 0.f) ? (d + __log2f(s)) * kLn2 : -INFINITY;
+    __syncthreads();  // sd/ss are rewritten for the next row
+  }
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" int fa_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
+                               void* stream) {
+  if (x == nullptr || y == nullptr) return FA_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0) return FA_ERR_INVALID_ARG;
+  if (rows > (1LL << 40) / cols) return FA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) & 3u) != 0 || (reinterpret_cast<uintptr_t>(y) & 3u) != 0 ||
+      (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0))
+    return FA_ERR_MISALIGNED;
+  int sms = 0;
+  if (fa::num_sms_of_current_device(&sms) != FA_OK) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cols <= fa::kWarpCols) {
+    const long long want = (rows + fa::kThreads / 32 - 1) / (fa::kThreads / 32);
+    const long long grid = want < 16LL * sms ? want : 16LL * sms;
+    fa::softmax_rows_warp<<<dim3(unsigned(grid)), dim3(fa::kThreads), 0, s>>>(x, y, lse, rows, cols);
+  } else {
+    const long long grid = rows < 8LL * sms ? rows : 8LL * sms;
+    fa::softmax_rows_cta<<<dim3(unsigned(grid)), dim3(fa::kThreads), 0, s>>>(x, y, lse, rows, cols);
+  }
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

@@ -178,10 +178,28 @@ int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                         int B, int H, int D, int num_pages, int page_size,
                         int max_pages_per_seq, float scale, void* stream);
 
+/*
+ * fa_softmax_rows - softmax of every row of a matrix, in two reads: the guide's
+ * "Expand: why multiplying by exp(d1 - d2) fixes it" (a running maximum d and
+ * a running sum s rescaled by exp(d_old - d_new) find Amax and the denominator
+ * in one read; a second read writes exp(a_i - Amax) / S).
+ *
+ * x    : device, fp32, [rows, cols], row-major; values finite or -inf.
+ * y    : device, fp32, [rows, cols]; written with the row softmax of x (may be
+ *        x itself: each element is read before it is written, in place).
+ * lse  : device, fp32, [rows]; written with ln(sum_j exp(x_ij)) (may be NULL).
+ *        A row of only -inf gets y = 0 and lse = -inf.
+ * rows >= 1, cols >= 1, rows * cols <= 2^40.  4-byte aligned pointers (16-byte
+ * aligned rows are read and written with vector accesses).
+ * Errors and asynchrony as for fa_fwd.
+ */
+int fa_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
+                    void* stream);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 1)
+#define FA_ABI_VERSION ((1 << 16) | 2)
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,7 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
-              "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged"):
+              "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows"):
         assert n in names
 
 
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16) | 1
+    assert lib.fa_abi_version() == (1 << 16) | 2
 
 
 def test_strerror_covers_every_status(lib):
@@ -173,3 +173,19 @@ def call_paged(**kw):
 ])
 def test_paged_bad_arguments_rejected_on_host(lib, kw, expect):
     assert call_paged(**kw) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(x=None), fa.FA_ERR_INVALID_ARG),
+    (dict(y=None), fa.FA_ERR_INVALID_ARG),
+    (dict(rows=0), fa.FA_ERR_INVALID_ARG),
+    (dict(cols=0), fa.FA_ERR_INVALID_ARG),
+    (dict(rows=1 << 40, cols=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(x=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(y=A + 1), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_softmax_bad_arguments_rejected_on_host(lib, kw, expect):
+    args = dict(x=A, y=A, lse=A, rows=4, cols=16)
+    args.update(kw)
+    assert lib.fa_softmax_rows(args["x"], args["y"], args["lse"], args["rows"], args["cols"], None) == expect
