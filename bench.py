@@ -302,6 +302,37 @@ def per_config(args, fa, flush, dev, peaks, check):
         torch.cuda.empty_cache()
     out.update(per_config_paged(fa, flush, dev, peaks, check))
     out.update(per_config_softmax(fa, flush, dev, peaks, check))
+    out.update(per_config_backward(fa, flush, dev, peaks, check))
+    return out
+
+
+def per_config_backward(fa, flush, dev, peaks, check):
+    """The backward pass (fa_bwd: preparation + dK/dV + dQ kernels) on the
+    causal 8K D128 workload.  TFLOPS count the five products a backward pass
+    needs (2.5 x the forward's flops); the kernels compute seven (S and dP
+    once for dK/dV and once for dQ)."""
+    import torch
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+    out = {}
+    w = WORKLOADS["causal_l8k_d128"]
+    q, k, v = make_inputs(w, dev)
+    g = torch.Generator(device=dev).manual_seed(11)
+    do = torch.randn(q.shape, generator=g, device=dev).to(torch.bfloat16)
+    o, lse = fa.forward(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    call = lambda: fa.backward(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv)
+    _time_launches([call], flush, 2)
+    ts = _time_launches([call], flush, 10)
+    check()
+    ms = statistics.median(ts)
+    flops = 2.5 * w.flops
+    tf = flops / (ms * 1e-3) / 1e12
+    out["backward_causal_l8k_d128"] = {"B": w.B, "H": w.H, "L": w.Lq, "D": w.D, "causal": True,
+                                       "ms": round(ms, 5), "TFLOPS": round(tf, 2),
+                                       "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+                                       "launches": 3, "flops_counted": flops}
+    del q, k, v, do, o, lse, dq, dk, dv
+    torch.cuda.empty_cache()
     return out
 
 

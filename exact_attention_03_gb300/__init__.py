@@ -20,7 +20,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGN
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
            "forward", "forward_host", "decode_noalloc", "decode_paged", "softmax_rows",
-           "EXPORTED_SYMBOLS"]
+           "backward", "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -56,6 +56,8 @@ _SIGS = {
                                            ctypes.c_float, ctypes.c_void_p]),
     "fa_softmax_rows": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
+    "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
+               + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -229,6 +231,34 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: Optional[flo
     if st != FA_OK:
         raise FlashAttentionError(st, "fa_fwd_decode_paged")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float] = None,
+             dq=None, dk=None, dv=None, stream=None):
+    """Gradients (dq, dk, dv) of <dout, O> through fa_bwd, for CUDA bf16
+    q, o, dout [B, H, Lq, D], k, v [B, H, Lk, D] and fp32 lse [B, H, Lq] from
+    forward() with the same causal flag and scale."""
+    import torch
+
+    B, H, Lq, D = q.shape
+    Lk = k.shape[2]
+    for name, t, shape in (("q", q, (B, H, Lq, D)), ("k", k, (B, H, Lk, D)), ("v", v, (B, H, Lk, D)),
+                           ("o", o, (B, H, Lq, D)), ("dout", dout, (B, H, Lq, D))):
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor of shape {shape}")
+    if tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or not lse.is_cuda:
+        raise ValueError("lse must be a CUDA fp32 tensor [B, H, Lq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    st = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D,
+                       float(scale), int(causal), _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def softmax_rows(x, out=None, lse=None, return_lse: bool = True, stream=None):

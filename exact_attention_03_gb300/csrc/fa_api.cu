@@ -215,6 +215,42 @@ int fa_last_device_error(void* stream, int* site) {
   return h[0];  // FA_OK, FA_ERR_TIMEOUT, or FA_ERR_INVALID_ARG (a page id out of range)
 }
 
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int D,
+           float scale, int causal, void* stream) {
+  // ---- host-side checks, before any CUDA call
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dout == nullptr ||
+      lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (causal && Lq != Lk) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                          static_cast<const void*>(dv)})
+    if (!fa::aligned(ptr, 16)) return FA_ERR_MISALIGNED;
+  if (!fa::aligned(lse, 4)) return FA_ERR_MISALIGNED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int* err = fa::error_word_ptr(dev);
+  if (err == nullptr) return FA_ERR_CUDA;
+  const size_t lq_pad = (size_t(Lq) + 127) / 128 * 128;
+  const size_t ws_bytes = 2 * size_t(BH) * lq_pad * sizeof(float);
+  void* ws = nullptr;
+  if (fa::workspace_alloc(&ws, ws_bytes, s) != FA_OK) return FA_ERR_CUDA;
+  const int st = fa::launch_backward(q, k, v, o, dout, lse, dq, dk, dv, int(BH), Lq, Lk, D, scale,
+                                     causal, static_cast<float*>(ws), err, s);
+  const bool freed = fa::workspace_free(ws, s) == FA_OK;
+  if (st == -2) return FA_ERR_UNSUPPORTED;
+  if (st != 0) return FA_ERR_CUDA;
+  return freed ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                         const int* block_table, const int* seq_lens, void* o, float* lse, int B,
                         int H, int D, int num_pages, int page_size, int max_pages_per_seq,

@@ -1,0 +1,540 @@
+// fa_backward_sm103.cu - attention backward pass (dQ, dK, dV) on sm_103a.
+//
+// "6.3 FlashAttention" (comfyai.app), "A simple implementation w/ C++" and
+// "Computation and GPU Memory": for training, the forward pass keeps no
+// attention weights; the backward pass recomputes them.  Given q, k, v, the
+// forward's output O and log-sum-exp (natural log) per query row, and the
+// output gradient dO, the gradients of <dO, O> are
+//     P  = exp(scale q k^T - LSE)           (the weights, recomputed)
+//     dV = P^T dO,   dP = dO V^T,   Dr = rowsum(dO * O) = rowsum(P * dP)
+//     dS = P * (dP - Dr),   dQ = scale dS K,   dK = scale dS^T Q.
+// Three kernels:
+//   fa_bwd_prep_kernel   Dr per query row, and LSE in base 2, into a workspace
+//                        padded to whole 128-row tiles (rows past Lq: Dr = 0,
+//                        LSE = +inf, so their weights are 0);
+//   fa_bwd_dkdv_kernel   one CTA per 128-key tile: walks the query tiles,
+//                        S^T = K Q^T and dP^T = V dO^T on the tensor cores into
+//                        TMEM, P^T and dS^T (bf16) written back over them by
+//                        four warps (one key row per thread), then
+//                        dV += P^T dO and dK += dS^T Q accumulate in TMEM;
+//   fa_bwd_dq_kernel     one CTA per 128-query tile: walks the key tiles,
+//                        S = Q K^T and dP = dO V^T, dS (bf16) over S, then
+//                        dQ += dS K in TMEM.
+// S and dP are computed twice (once per kernel): no atomics, deterministic
+// results.  TMEM (512 columns): dK/dV kernel S^T [0,128) dP^T [128,256)
+// dV [256,256+D) dK [256+D,256+2D); dQ kernel S [0,128) dP [128,256)
+// dQ [256,256+D).  Warps: 0 = TMA producer, 1 = TMEM allocation + MMA issue,
+// 2-5 = the element-wise work and the epilogue (TMEM lane quarter = warp % 4).
+// Every wait is bounded (the same routine as the forward kernels).
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace fa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwCfg {
+  static constexpr int kTileBytes = 128 * D * 2;        // one 128-row tile (one TMA box)
+  static constexpr int kSubBytes = 128 * 128;           // one 64-column block of a tile
+  static constexpr int kStages = D == 64 ? 4 : 2;       // ring of (two-tile) stages
+  static constexpr int kFixedOff = 0;                   // the CTA's own two tiles
+  static constexpr int kRingOff = 2 * kTileBytes;       // stage s: tiles at +2s, +2s+1
+  static constexpr int kBarOff = kRingOff + kStages * 2 * kTileBytes;
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+};
+
+struct BwParams {
+  __nv_bfloat16* out_a;   // dK (dkdv kernel) or dQ (dq kernel)
+  __nv_bfloat16* out_b;   // dV (dkdv kernel)
+  const float* lse2;      // [BH][Lq_pad]: LSE * log2(e), +inf past Lq
+  const float* drow;      // [BH][Lq_pad]: rowsum(dO * O), 0 past Lq
+  int* err;
+  int BH, Lq, Lk, Lq_pad;
+  int causal;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0; it < (1u << 22); ++it) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((it & 15u) == 15u && globaltimer_ns() - t0 > 50000000ull) return;  // 50 ms
+  }
+}
+
+// ---------------------------------------------------------------- preparation
+
+template <int D>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* o,
+                                                          const __nv_bfloat16* dout,
+                                                          const float* lse, float* lse2,
+                                                          float* drow, int BH, int Lq,
+                                                          int Lq_pad) {
+  // D/8 lanes per row, 16 bytes of O and dO per lane
+  constexpr int G = D / 8;
+  const long long n = (long long)BH * Lq_pad;
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gid / G;
+  const int li = int(gid % G);
+  const bool in = row < n;   // every lane stays for the shuffles below
+  const int bh = in ? int(row / Lq_pad) : 0;
+  const int r = in ? int(row % Lq_pad) : Lq;
+  float acc = 0.f;
+  if (r < Lq) {
+    const size_t base = (size_t(bh) * Lq + r) * D + 8 * li;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + base);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + base);
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(wa[e] << 16), __uint_as_float(wb[e] << 16), acc);
+      acc = fmaf(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wb[e] & 0xffff0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (in && li == 0) {
+    drow[row] = acc;
+    lse2[row] = r < Lq ? lse[size_t(bh) * Lq + r] * kLog2e : INFINITY;
+  }
+}
+
+// ---------------------------------------------------------------- shared pieces
+
+// operand descriptors: a [128 x D] tile as the K-major operand of a product
+// over D, or as the MN-major operand (K = its 128 rows, N = D) of a product
+// over its rows
+template <int D>
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
+  constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);
+  return sdesc_at(kDesc, tile + (kk >> 2) * BwCfg<D>::kSubBytes + (kk & 3) * 32);
+}
+template <int D>
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
+  constexpr uint64_t kDesc = sdesc_sw128(0, BwCfg<D>::kSubBytes, 1024);
+  return sdesc_at(kDesc, tile + kk * 16 * 128);
+}
+
+// element-wise step on one 128-wide row held in TMEM (S^T/dP^T rows of keys, or
+// S/dP rows of queries): chunk c covers columns 32c .. 32c+31 of both; the
+// weights p and dS = p (dP - Dr) are packed to bf16 and written back over the
+// consumed columns (p over S at [16c, 16c+16), dS over dP at [128+16c, ...)).
+// `valid(e)` and `coef(e, lse2, dr)` give the mask and per-column terms.
+template <bool WRITE_P, class Valid, class Coef>
+__device__ __forceinline__ void weights_row(uint32_t tS, uint32_t tdP, float c, Valid valid, Coef coef) {
+#pragma unroll 1
+  for (int ch = 0; ch < 4; ++ch) {
+    float s[32], dp[32];
+    tmem_ld32_sync(tS + 32 * ch, s);
+    tmem_ld32_sync(tdP + 32 * ch, dp);
+    uint32_t wp[16], wd[16];
+#pragma unroll
+    for (int e2 = 0; e2 < 16; ++e2) {
+      float pv[2], dv[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = 32 * ch + 2 * e2 + h;
+        float l2, dr;
+        coef(e, l2, dr);
+        const float p = valid(e) ? ex2_approx(fmaf(s[2 * e2 + h], c, -l2)) : 0.f;
+        pv[h] = p;
+        dv[h] = p * (dp[2 * e2 + h] - dr);
+      }
+      wp[e2] = pack_bf16x2(pv[0], pv[1]);
+      wd[e2] = pack_bf16x2(dv[0], dv[1]);
+    }
+    if (WRITE_P) tmem_st16(tS + 16 * ch, wp);
+    tmem_st16(tdP + 16 * ch, wd);
+  }
+  tmem_st_wait();
+}
+
+// ---------------------------------------------------------------- dK, dV
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const BwParams p) {
+  using C = BwCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sK = base + C::kFixedOff, sV = sK + C::kTileBytes;
+  auto st_q = [&](int s) { return base + C::kRingOff + (2 * s) * C::kTileBytes; };
+  auto st_do = [&](int s) { return base + C::kRingOff + (2 * s + 1) * C::kTileBytes; };
+  const uint32_t sBar = base + C::kBarOff;
+  auto bar_full = [&](int s) { return sBar + 8 * s; };
+  auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
+  const uint32_t bar_kv = sBar + 128, bar_s = sBar + 136, bar_p = sBar + 144, bar_done = sBar + 152;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int jt = int(blockIdx.x) / p.BH;      // key tile (the most query tiles first when causal)
+  const int bh = int(blockIdx.x) % p.BH;
+  const int nq_all = (p.Lq + 127) / 128;
+  const int i0 = p.causal ? jt : 0;           // causal: queries q >= key, so query tiles >= jt
+  const int n = nq_all - i0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
+      tma_load_tile(sK, &tmK, bar_kv, jt * 128, bh);
+      tma_load_tile(sV, &tmV, bar_kv, jt * 128, bh);
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int s = it % C::kStages, use = it / C::kStages;
+        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
+        tma_load_tile(st_q(s), &tmQ, bar_full(s), (i0 + it) * 128, bh);
+        tma_load_tile(st_do(s), &tmDO, bar_full(s), (i0 + it) * 128, bh);
+        ++issued;
+      }
+      drain(bar_kv, 0);
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
+        drain(bar_full(s), (last / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_kv, 0, abort_flag, p.err, kSiteMmaK);
+      for (int it = 0; it < n && ok; ++it) {
+        const int s = it % C::kStages;
+        if (!(ok = mbar_wait(bar_full(s), (it / C::kStages) & 1, abort_flag, p.err, kSiteMmaQ))) break;
+        tc_fence_after();
+        // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 128 queries, K = D)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+        if (!(ok = mbar_wait(bar_p, it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        tc_fence_after();
+        // dV += P^T dO and dK += dS^T Q (M = 128 keys, N = D, K = 128 queries)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256, tmem + kk * 8, desc_mnmajor<D>(st_do(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256 + D, tmem + 128 + kk * 8, desc_mnmajor<D>(st_q(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar_empty(s));
+      }
+      umma_commit(bar_done);
+      drain(bar_done, 0);
+    }
+  } else {
+    // element-wise: one key row per thread
+    const int g = warp & 3;
+    const int r = g * 32 + lane;
+    const int key = jt * 128 + r;
+    const uint32_t lane_off = uint32_t(g * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
+    bool ok = true;
+    const float* l2row = p.lse2 + size_t(bh) * p.Lq_pad;
+    const float* drrow = p.drow + size_t(bh) * p.Lq_pad;
+    for (int it = 0; it < n && ok; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = (i0 + it) * 128;
+      const bool key_ok = key < p.Lk;
+      const bool diag = p.causal && (i0 + it) == jt;
+      weights_row<true>(
+          tS, tdP, p.scale_log2,
+          [&](int e) { return key_ok && (!diag || key <= q0 + e); },
+          [&](int e, float& l2, float& dr) {
+            l2 = __ldg(l2row + q0 + e);
+            dr = __ldg(drrow + q0 + e);
+          });
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    // epilogue: dV and scale * dK rows of this key.  The TMEM loads are
+    // warp-collective: every lane takes part, only the stores are predicated.
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag, p.err, kSiteSoftmaxO));
+    if (ok) {
+      tc_fence_after();
+      const bool valid = key < p.Lk;
+      const size_t orow = (size_t(bh) * p.Lk + (valid ? key : 0)) * D;
+#pragma unroll 1
+      for (int part = 0; part < 2; ++part) {
+        __nv_bfloat16* dst = part == 0 ? p.out_b : p.out_a;  // dV, then dK
+        const float mul = part == 0 ? 1.f : p.scale;
+#pragma unroll 1
+        for (int cc = 0; cc < D; cc += 32) {
+          float v[32];
+          tmem_ld32_sync(tmem + lane_off + 256 + part * D + cc, v);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + orow + cc);
+          if (valid) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8)
+              d4[q8] = make_uint4(pack_bf16x2(v[8 * q8] * mul, v[8 * q8 + 1] * mul),
+                                  pack_bf16x2(v[8 * q8 + 2] * mul, v[8 * q8 + 3] * mul),
+                                  pack_bf16x2(v[8 * q8 + 4] * mul, v[8 * q8 + 5] * mul),
+                                  pack_bf16x2(v[8 * q8 + 6] * mul, v[8 * q8 + 7] * mul));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const BwParams p) {
+  using C = BwCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + C::kFixedOff, sDO = sQ + C::kTileBytes;
+  auto st_k = [&](int s) { return base + C::kRingOff + (2 * s) * C::kTileBytes; };
+  auto st_v = [&](int s) { return base + C::kRingOff + (2 * s + 1) * C::kTileBytes; };
+  const uint32_t sBar = base + C::kBarOff;
+  auto bar_full = [&](int s) { return sBar + 8 * s; };
+  auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
+  const uint32_t bar_q = sBar + 128, bar_s = sBar + 136, bar_p = sBar + 144, bar_done = sBar + 152;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq_all = (p.Lq + 127) / 128;
+  const int itile = nq_all - 1 - int(blockIdx.x) / p.BH;  // the most key tiles first when causal
+  const int bh = int(blockIdx.x) % p.BH;
+  const int nk_all = (p.Lk + 127) / 128;
+  const int n = p.causal ? min(nk_all, itile + 1) : nk_all;   // causal: keys <= query
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    mbar_init(bar_q, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
+      tma_load_tile(sQ, &tmQ, bar_q, itile * 128, bh);
+      tma_load_tile(sDO, &tmDO, bar_q, itile * 128, bh);
+      int issued = 0;
+      for (int it = 0; it < n; ++it) {
+        const int s = it % C::kStages, use = it / C::kStages;
+        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
+        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
+        tma_load_tile(st_k(s), &tmK, bar_full(s), it * 128, bh);
+        tma_load_tile(st_v(s), &tmV, bar_full(s), it * 128, bh);
+        ++issued;
+      }
+      drain(bar_q, 0);
+      for (int s = 0; s < C::kStages && s < issued; ++s) {
+        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
+        drain(bar_full(s), (last / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
+      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ);
+      for (int it = 0; it < n && ok; ++it) {
+        const int s = it % C::kStages;
+        if (!(ok = mbar_wait(bar_full(s), (it / C::kStages) & 1, abort_flag, p.err, kSiteMmaK))) break;
+        tc_fence_after();
+        // S = Q K^T and dP = dO V^T (M = 128 queries, N = 128 keys, K = D)
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_s);
+        if (!(ok = mbar_wait(bar_p, it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        tc_fence_after();
+        // dQ += dS K (M = 128 queries, N = D, K = 128 keys); dS sits over dP
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256, tmem + 128 + kk * 8, desc_mnmajor<D>(st_k(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar_empty(s));
+      }
+      umma_commit(bar_done);
+      drain(bar_done, 0);
+    }
+  } else {
+    // element-wise: one query row per thread
+    const int g = warp & 3;
+    const int r = g * 32 + lane;
+    const int qrow = itile * 128 + r;
+    const uint32_t lane_off = uint32_t(g * 32) << 16;
+    const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
+    const float l2 = p.lse2[size_t(bh) * p.Lq_pad + qrow];
+    const float dr = p.drow[size_t(bh) * p.Lq_pad + qrow];
+    bool ok = true;
+    for (int it = 0; it < n && ok; ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      tc_fence_after();
+      const int k0 = it * 128;
+      weights_row<false>(
+          tS, tdP, p.scale_log2,
+          [&](int e) { return k0 + e < p.Lk && (!p.causal || k0 + e <= qrow); },
+          [&](int, float& l2_, float& dr_) {
+            l2_ = l2;
+            dr_ = dr;
+          });
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    // epilogue: scale * dQ row (warp-collective TMEM loads, predicated stores)
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag, p.err, kSiteSoftmaxO));
+    if (ok) {
+      tc_fence_after();
+      const bool valid = qrow < p.Lq;
+      const size_t orow = (size_t(bh) * p.Lq + (valid ? qrow : 0)) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D; cc += 32) {
+        float v[32];
+        tmem_ld32_sync(tmem + lane_off + 256 + cc, v);
+        uint4* d4 = reinterpret_cast<uint4*>(p.out_a + orow + cc);
+        if (valid) {
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8)
+            d4[q8] = make_uint4(pack_bf16x2(v[8 * q8] * p.scale, v[8 * q8 + 1] * p.scale),
+                                pack_bf16x2(v[8 * q8 + 2] * p.scale, v[8 * q8 + 3] * p.scale),
+                                pack_bf16x2(v[8 * q8 + 4] * p.scale, v[8 * q8 + 5] * p.scale),
+                                pack_bf16x2(v[8 * q8 + 6] * p.scale, v[8 * q8 + 7] * p.scale));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, float scale,
+                 int causal, float* ws, int* err, cudaStream_t stream) {
+  using C = BwCfg<D>;
+  CUtensorMap mq, mk, mv, mdo;
+  int st = make_tensor_map_bf16(&mq, q, BH, Lq, D);
+  if (st == 0) st = make_tensor_map_bf16(&mk, k, BH, Lk, D);
+  if (st == 0) st = make_tensor_map_bf16(&mv, v, BH, Lk, D);
+  if (st == 0) st = make_tensor_map_bf16(&mdo, dout, BH, Lq, D);
+  if (st != 0) return st;
+  BwParams p;
+  p.BH = BH;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.Lq_pad = (Lq + 127) / 128 * 128;
+  p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.err = err;
+  float* lse2 = ws;
+  float* drow = ws + size_t(BH) * p.Lq_pad;
+  p.lse2 = lse2;
+  p.drow = drow;
+  {
+    const long long threads = (long long)BH * p.Lq_pad * (D / 8);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return -2;
+    fa_bwd_prep_kernel<D><<<dim3(unsigned(blocks)), dim3(256), 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, lse2, drow,
+        BH, Lq, p.Lq_pad);
+    if (cudaGetLastError() != cudaSuccess) return -4;
+  }
+  if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmemBytes) != cudaSuccess)
+    return -4;
+  const long long nk = (long long)((Lk + 127) / 128) * BH;
+  const long long nq = (long long)((Lq + 127) / 128) * BH;
+  if (nk > 0x7fffffffLL || nq > 0x7fffffffLL) return -2;
+  p.out_a = static_cast<__nv_bfloat16*>(dk);
+  p.out_b = static_cast<__nv_bfloat16*>(dv);
+  fa_bwd_dkdv_kernel<D><<<dim3(unsigned(nk)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  p.out_a = static_cast<__nv_bfloat16*>(dq);
+  p.out_b = nullptr;
+  fa_bwd_dq_kernel<D><<<dim3(unsigned(nq)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+
+}  // namespace
+
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, int D,
+                    float scale, int causal, float* workspace, int* err, cudaStream_t stream) {
+  if (D == 64)
+    return launch_bwd_d<64>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err, stream);
+  if (D == 128)
+    return launch_bwd_d<128>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err, stream);
+  return -2;
+}
+
+}  // namespace fa

@@ -47,6 +47,12 @@ int launch_decode_paged(const void* q, const void* k_cache, const void* v_cache,
                         int H, int D, int num_pages, int page_size, int max_pages, float scale,
                         int n_split, float* workspace, int* err, cudaStream_t stream);
 
+// Backward pass (fa_bwd): arguments already validated; `workspace` holds
+// 2 * BH * roundup(Lq, 128) floats.  Returns 0, -2 or -4 (or a tensor-map error).
+int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, int D,
+                    float scale, int causal, float* workspace, int* err, cudaStream_t stream);
+
 int num_sms_of_current_device(int* num_sms);
 
 // Workspace memory, stream-ordered on `stream`, from the library's pool of the

@@ -196,10 +196,31 @@ int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,
 int fa_softmax_rows(const float* x, float* y, float* lse, long long rows, int cols,
                     void* stream);
 
+/*
+ * fa_bwd - attention backward pass with recomputation ("6.3 FlashAttention",
+ * "A simple implementation w/ C++": the weights are not saved by the forward
+ * pass but recomputed here).  Computes the gradients of <dout, O> with respect
+ * to q, k and v, where O = softmax(scale q k^T [causal]) v is fa_fwd's output:
+ * dv = P^T dout, dq = scale dS k, dk = scale dS^T q with
+ * P = exp(scale q k^T - lse), dS = P * (dout v^T - rowsum(dout * O)).
+ *
+ * q, o, dout : device, bf16, [B, H, Lq, D]; k, v: [B, H, Lk, D] (contiguous).
+ *              o is fa_fwd's output for these q, k, v, scale and causal flag.
+ * lse        : device, fp32, [B, H, Lq]: fa_fwd's log-sum-exp (natural log).
+ * dq, dk, dv : device, bf16, shaped like q, k, v; written.
+ * Argument rules as for fa_fwd (D in {64, 128}, causal needs Lq == Lk; every
+ * bf16 pointer 16-byte aligned, lse 4-byte aligned).  Workspace:
+ * 2 * B * H * roundup(Lq, 128) * 4 bytes from the library's pool (see fa_fwd).
+ * Errors and asynchrony as for fa_fwd.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+           int D, float scale, int causal, void* stream);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 2)
+#define FA_ABI_VERSION ((1 << 16) | 3)
 
 #ifdef __cplusplus
 }

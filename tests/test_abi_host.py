@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16) | 2
+    assert lib.fa_abi_version() == (1 << 16) | 3
 
 
 def test_strerror_covers_every_status(lib):
@@ -189,3 +189,26 @@ def test_softmax_bad_arguments_rejected_on_host(lib, kw, expect):
     args = dict(x=A, y=A, lse=A, rows=4, cols=16)
     args.update(kw)
     assert lib.fa_softmax_rows(args["x"], args["y"], args["lse"], args["rows"], args["cols"], None) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(do=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dq=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Lk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=1, Lq=64, Lk=128), fa.FA_ERR_UNSUPPORTED),
+    (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(dk=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_bwd_bad_arguments_rejected_on_host(lib, kw, expect):
+    a = dict(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, Lq=128, Lk=128, D=128,
+             scale=0.1, causal=0)
+    a.update(kw)
+    assert lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
+                      a["B"], a["H"], a["Lq"], a["Lk"], a["D"], a["scale"], a["causal"], None) == expect
