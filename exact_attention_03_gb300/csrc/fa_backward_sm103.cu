@@ -44,7 +44,8 @@ struct BwCfg {
   static constexpr int kStages = D == 64 ? 4 : 2;       // ring of (two-tile) stages
   static constexpr int kFixedOff = 0;                   // the CTA's own two tiles
   static constexpr int kRingOff = 2 * kTileBytes;       // stage s: tiles at +2s, +2s+1
-  static constexpr int kBarOff = kRingOff + kStages * 2 * kTileBytes;
+  static constexpr int kVecOff = kRingOff + kStages * 2 * kTileBytes;  // per stage: 128 LSE2 + 128 Dr
+  static constexpr int kBarOff = kVecOff + kStages * 1024;
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
 };
 
@@ -58,6 +59,13 @@ struct BwParams {
   int causal;
   float scale, scale_log2;
 };
+
+// 1-D bulk copy global -> shared, completing `bytes` on `bar` (16-byte aligned, multiple of 16)
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -169,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sK = base + C::kFixedOff, sV = sK + C::kTileBytes;
   auto st_q = [&](int s) { return base + C::kRingOff + (2 * s) * C::kTileBytes; };
   auto st_do = [&](int s) { return base + C::kRingOff + (2 * s + 1) * C::kTileBytes; };
+  auto st_vec = [&](int s) { return base + C::kVecOff + s * 1024; };
   const uint32_t sBar = base + C::kBarOff;
   auto bar_full = [&](int s) { return sBar + 8 * s; };
   auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
@@ -213,9 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n; ++it) {
         const int s = it % C::kStages, use = it / C::kStages;
         if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
-        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
+        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes + 1024);
         tma_load_tile(st_q(s), &tmQ, bar_full(s), (i0 + it) * 128, bh);
         tma_load_tile(st_do(s), &tmDO, bar_full(s), (i0 + it) * 128, bh);
+        const size_t voff = size_t(bh) * p.Lq_pad + size_t(i0 + it) * 128;
+        bulk_load(st_vec(s), p.lse2 + voff, 512, bar_full(s));
+        bulk_load(st_vec(s) + 512, p.drow + voff, 512, bar_full(s));
         ++issued;
       }
       drain(bar_kv, 0);
@@ -265,8 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(g * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
     bool ok = true;
-    const float* l2row = p.lse2 + size_t(bh) * p.Lq_pad;
-    const float* drrow = p.drow + size_t(bh) * p.Lq_pad;
     for (int it = 0; it < n && ok; ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
@@ -274,12 +284,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int q0 = (i0 + it) * 128;
       const bool key_ok = key < p.Lk;
       const bool diag = p.causal && (i0 + it) == jt;
+      // the stage's LSE2 / Dr slices landed with its Q, dO tiles: wait on that
+      // barrier too (already complete; it cannot move on before this group
+      // releases the stage) so that the copied values are visible here
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_full(it % C::kStages), (it / C::kStages) & 1,
+                                             abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStages) - base));
+      const float* vdr = vl2 + 128;
       weights_row<true>(
           tS, tdP, p.scale_log2,
           [&](int e) { return key_ok && (!diag || key <= q0 + e); },
           [&](int e, float& l2, float& dr) {
-            l2 = __ldg(l2row + q0 + e);
-            dr = __ldg(drrow + q0 + e);
+            l2 = vl2[e];
+            dr = vdr[e];
           });
       tc_fence_before();
       mbar_arrive(bar_p);
