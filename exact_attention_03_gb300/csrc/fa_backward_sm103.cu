@@ -15,16 +15,26 @@
 //   fa_bwd_dkdv_kernel   one CTA per 128-key tile: walks the query tiles,
 //                        S^T = K Q^T and dP^T = V dO^T on the tensor cores into
 //                        TMEM, P^T and dS^T (bf16) written back over them by
-//                        four warps (one key row per thread), then
+//                        the element-wise warps (one key row per thread), then
 //                        dV += P^T dO and dK += dS^T Q accumulate in TMEM;
 //   fa_bwd_dq_kernel     one CTA per 128-query tile: walks the key tiles,
-//                        S = Q K^T and dP = dO V^T, dS (bf16) over S, then
+//                        S = Q K^T and dP = dO V^T, dS (bf16) over dP, then
 //                        dQ += dS K in TMEM.
 // S and dP are computed twice (once per kernel): no atomics, deterministic
 // results.  TMEM (512 columns): dK/dV kernel S^T [0,128) dP^T [128,256)
 // dV [256,256+D) dK [256+D,256+2D); dQ kernel S [0,128) dP [128,256)
-// dQ [256,256+D).  Warps: 0 = TMA producer, 1 = TMEM allocation + MMA issue,
-// 2-5 = the element-wise work and the epilogue (TMEM lane quarter = warp % 4).
+// dQ [256,256+D).
+// Each tile's 128 columns (queries in dK/dV, keys in dQ) are taken in two
+// halves of 64 with their own products, barriers and warp group, so that the
+// tensor core computes one half while the element-wise work of the other runs:
+//   S_0 dP_0 S_1 dP_1 | G_0 S'_0 dP'_0 G_1 S'_1 dP'_1 | G'_0 ...
+// (G_h = the gradient products that consume half h; ' = the next tile).  Half
+// h's bf16 results are packed into columns [64h, 64h+32) of the S and dP
+// regions, inside the columns that half itself consumed, and the next tile's
+// S_h is issued after G_h: tcgen05.mma operations from one thread execute in
+// order.  Warps: 0 = TMA producer, 1 = TMEM allocation + MMA issue, 2-5 = half
+// 0 and 6-9 = half 1 of the element-wise work and the epilogue (TMEM lane
+// quarter = warp % 4), so each SM sub-partition runs two element-wise warps.
 // Every wait is bounded (the same routine as the forward kernels).
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -34,7 +44,7 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
@@ -128,38 +138,80 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return sdesc_at(kDesc, tile + kk * 16 * 128);
 }
 
-// element-wise step on one 128-wide row held in TMEM (S^T/dP^T rows of keys, or
-// S/dP rows of queries): chunk c covers columns 32c .. 32c+31 of both; the
-// weights p and dS = p (dP - Dr) are packed to bf16 and written back over the
-// consumed columns (p over S at [16c, 16c+16), dS over dP at [128+16c, ...)).
-// `valid(e)` and `coef(e, lse2, dr)` give the mask and per-column terms.
+// 32 columns at each of two TMEM addresses, with one wait for both loads
+__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
+  uint32_t ra[32], rb[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]),
+        "=r"(ra[7]), "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]),
+        "=r"(ra[14]), "=r"(ra[15]), "=r"(ra[16]), "=r"(ra[17]), "=r"(ra[18]), "=r"(ra[19]),
+        "=r"(ra[20]), "=r"(ra[21]), "=r"(ra[22]), "=r"(ra[23]), "=r"(ra[24]), "=r"(ra[25]),
+        "=r"(ra[26]), "=r"(ra[27]), "=r"(ra[28]), "=r"(ra[29]), "=r"(ra[30]), "=r"(ra[31]),
+        "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]),
+        "=r"(rb[7]), "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]),
+        "=r"(rb[14]), "=r"(rb[15]), "=r"(rb[16]), "=r"(rb[17]), "=r"(rb[18]), "=r"(rb[19]),
+        "=r"(rb[20]), "=r"(rb[21]), "=r"(rb[22]), "=r"(rb[23]), "=r"(rb[24]), "=r"(rb[25]),
+        "=r"(rb[26]), "=r"(rb[27]), "=r"(rb[28]), "=r"(rb[29]), "=r"(rb[30]), "=r"(rb[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    a[i] = __uint_as_float(ra[i]);
+    b[i] = __uint_as_float(rb[i]);
+  }
+}
+
+// element-wise step on half h (columns 64h .. 64h+63) of one 128-wide row held
+// in TMEM (S^T/dP^T rows of keys, or S/dP rows of queries), in two chunks of 32
+// columns; the weights p and dS = p (dP - Dr) are packed to bf16 and written
+// back into the half's own consumed columns: chunk c of the half goes to
+// [64h + 16c, 64h + 16c + 16) of the S and dP regions.  `valid(e)` and
+// `coef(e, lse2, dr)` give the mask and the per-column terms of column e.
 template <bool WRITE_P, class Valid, class Coef>
-__device__ __forceinline__ void weights_row(uint32_t tS, uint32_t tdP, float c, Valid valid, Coef coef) {
+__device__ __forceinline__ void weights_half(uint32_t tS, uint32_t tdP, float c, int h, Valid valid, Coef coef) {
 #pragma unroll 1
-  for (int ch = 0; ch < 4; ++ch) {
+  for (int ch = 0; ch < 2; ++ch) {
+    const int col = 64 * h + 32 * ch;
     float s[32], dp[32];
-    tmem_ld32_sync(tS + 32 * ch, s);
-    tmem_ld32_sync(tdP + 32 * ch, dp);
+    tmem_ld32x2_sync(tS + col, tdP + col, s, dp);
     uint32_t wp[16], wd[16];
 #pragma unroll
     for (int e2 = 0; e2 < 16; ++e2) {
       float pv[2], dv[2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int e = 32 * ch + 2 * e2 + h;
+      for (int k = 0; k < 2; ++k) {
+        const int e = col + 2 * e2 + k;
         float l2, dr;
         coef(e, l2, dr);
-        const float p = valid(e) ? ex2_approx(fmaf(s[2 * e2 + h], c, -l2)) : 0.f;
-        pv[h] = p;
-        dv[h] = p * (dp[2 * e2 + h] - dr);
+        const float p = valid(e) ? ex2_approx(fmaf(s[2 * e2 + k], c, -l2)) : 0.f;
+        pv[k] = p;
+        dv[k] = p * (dp[2 * e2 + k] - dr);
       }
       wp[e2] = pack_bf16x2(pv[0], pv[1]);
       wd[e2] = pack_bf16x2(dv[0], dv[1]);
     }
-    if (WRITE_P) tmem_st16(tS + 16 * ch, wp);
-    tmem_st16(tdP + 16 * ch, wd);
+    if (WRITE_P) tmem_st16(tS + 64 * h + 16 * ch, wp);
+    tmem_st16(tdP + 64 * h + 16 * ch, wd);
   }
   tmem_st_wait();
+}
+
+// bf16 store of 32 fp32 values times `mul` to 16-byte aligned global memory
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], float mul) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q8 = 0; q8 < 4; ++q8)
+    d4[q8] = make_uint4(pack_bf16x2(v[8 * q8] * mul, v[8 * q8 + 1] * mul),
+                        pack_bf16x2(v[8 * q8 + 2] * mul, v[8 * q8 + 3] * mul),
+                        pack_bf16x2(v[8 * q8 + 4] * mul, v[8 * q8 + 5] * mul),
+                        pack_bf16x2(v[8 * q8 + 6] * mul, v[8 * q8 + 7] * mul));
 }
 
 // ---------------------------------------------------------------- dK, dV
@@ -181,7 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sBar = base + C::kBarOff;
   auto bar_full = [&](int s) { return sBar + 8 * s; };
   auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
-  const uint32_t bar_kv = sBar + 128, bar_s = sBar + 136, bar_p = sBar + 144, bar_done = sBar + 152;
+  const uint32_t bar_kv = sBar + 128, bar_done = sBar + 168;
+  auto bar_s = [&](int h) { return sBar + 136 + 8 * h; };
+  auto bar_p = [&](int h) { return sBar + 152 + 8 * h; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
@@ -198,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_kv, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar_s(h), 1);
+      mbar_init(bar_p(h), 128);
+    }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -238,95 +294,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_kv, 0, abort_flag, p.err, kSiteMmaK);
+      // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (M = 128 keys, N = 64 queries
+      // 64h.., K = D); rows 64h.. of a tile start 64 x 128 bytes into each of
+      // its 64-column blocks
+      auto issue_s = [&](int s, int h) {
+        const uint32_t roff = uint32_t(h) * 64 * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 64 * h, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s) + roff, kk), kIdS,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128 + 64 * h, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s) + roff, kk), kIdS,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar_s(h));
+      };
+      // dV += P^T_h dO_h and dK += dS^T_h Q_h (M = 128 keys, N = D, K = 64 queries)
+      auto issue_grad = [&](int s, int h, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts(tmem + 256, tmem + 64 * h + kk * 8, desc_mnmajor<D>(st_do(s), 4 * h + kk), kIdTS,
+                  (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts(tmem + 256 + D, tmem + 128 + 64 * h + kk * 8, desc_mnmajor<D>(st_q(s), 4 * h + kk),
+                  kIdTS, (first && kk == 0) ? 0u : 1u);
+      };
+      bool ok = mbar_wait(bar_kv, 0, abort_flag, p.err, kSiteMmaK) &&
+                mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaQ);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
       for (int it = 0; it < n && ok; ++it) {
-        const int s = it % C::kStages;
-        if (!(ok = mbar_wait(bar_full(s), (it / C::kStages) & 1, abort_flag, p.err, kSiteMmaQ))) break;
+        const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
+        const bool more = it + 1 < n;
+        if (!(ok = mbar_wait(bar_p(0), it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (M = 128 keys, N = 128 queries, K = D)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s), kk), kIdSS, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s), kk), kIdSS, kk > 0 ? 1u : 0u);
-        umma_commit(bar_s);
-        if (!(ok = mbar_wait(bar_p, it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        issue_grad(s, 0, it == 0);
+        if (more) {
+          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaQ))) break;
+          tc_fence_after();
+          issue_s(s2, 0);
+        }
+        if (!(ok = mbar_wait(bar_p(1), it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // dV += P^T dO and dK += dS^T Q (M = 128 keys, N = D, K = 128 queries)
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256, tmem + kk * 8, desc_mnmajor<D>(st_do(s), kk), kIdTS,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + D, tmem + 128 + kk * 8, desc_mnmajor<D>(st_q(s), kk), kIdTS,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+        issue_grad(s, 1, false);
         umma_commit(bar_empty(s));
+        if (more) issue_s(s2, 1);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
     }
   } else {
-    // element-wise: one key row per thread
-    const int g = warp & 3;
+    // element-wise: one key row per thread, queries 64h .. 64h+63 of each tile
+    const int g = warp & 3, h = (warp - 2) >> 2;
     const int r = g * 32 + lane;
     const int key = jt * 128 + r;
     const uint32_t lane_off = uint32_t(g * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(h), it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
       const int q0 = (i0 + it) * 128;
       const bool key_ok = key < p.Lk;
       const bool diag = p.causal && (i0 + it) == jt;
       // the stage's LSE2 / Dr slices landed with its Q, dO tiles: wait on that
-      // barrier too (already complete; it cannot move on before this group
-      // releases the stage) so that the copied values are visible here
+      // barrier too (already complete; it cannot move on before both groups
+      // release the stage) so that the copied values are visible here
       ok = __all_sync(0xffffffffu, mbar_wait(bar_full(it % C::kStages), (it / C::kStages) & 1,
                                              abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStages) - base));
       const float* vdr = vl2 + 128;
-      weights_row<true>(
-          tS, tdP, p.scale_log2,
+      weights_half<true>(
+          tS, tdP, p.scale_log2, h,
           [&](int e) { return key_ok && (!diag || key <= q0 + e); },
           [&](int e, float& l2, float& dr) {
             l2 = vl2[e];
             dr = vdr[e];
           });
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(bar_p(h));
     }
-    // epilogue: dV and scale * dK rows of this key.  The TMEM loads are
-    // warp-collective: every lane takes part, only the stores are predicated.
+    // epilogue: group 0 writes the dV row of this key, group 1 scale * dK.
+    // The TMEM loads are warp-collective: every lane takes part, only the
+    // stores are predicated.
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag, p.err, kSiteSoftmaxO));
     if (ok) {
       tc_fence_after();
       const bool valid = key < p.Lk;
       const size_t orow = (size_t(bh) * p.Lk + (valid ? key : 0)) * D;
+      __nv_bfloat16* dst = (h == 0 ? p.out_b : p.out_a) + orow;
+      const float mul = h == 0 ? 1.f : p.scale;
 #pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        __nv_bfloat16* dst = part == 0 ? p.out_b : p.out_a;  // dV, then dK
-        const float mul = part == 0 ? 1.f : p.scale;
-#pragma unroll 1
-        for (int cc = 0; cc < D; cc += 32) {
-          float v[32];
-          tmem_ld32_sync(tmem + lane_off + 256 + part * D + cc, v);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + orow + cc);
-          if (valid) {
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8)
-              d4[q8] = make_uint4(pack_bf16x2(v[8 * q8] * mul, v[8 * q8 + 1] * mul),
-                                  pack_bf16x2(v[8 * q8 + 2] * mul, v[8 * q8 + 3] * mul),
-                                  pack_bf16x2(v[8 * q8 + 4] * mul, v[8 * q8 + 5] * mul),
-                                  pack_bf16x2(v[8 * q8 + 6] * mul, v[8 * q8 + 7] * mul));
-          }
-        }
+      for (int cc = 0; cc < D; cc += 32) {
+        float v[32];
+        tmem_ld32_sync(tmem + lane_off + 256 + h * D + cc, v);
+        if (valid) store_row32(dst + cc, v, mul);
       }
     }
   }
@@ -356,7 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sBar = base + C::kBarOff;
   auto bar_full = [&](int s) { return sBar + 8 * s; };
   auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
-  const uint32_t bar_q = sBar + 128, bar_s = sBar + 136, bar_p = sBar + 144, bar_done = sBar + 152;
+  const uint32_t bar_q = sBar + 128, bar_done = sBar + 168;
+  auto bar_s = [&](int h) { return sBar + 136 + 8 * h; };
+  auto bar_p = [&](int h) { return sBar + 152 + 8 * h; };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
@@ -373,8 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 128);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar_s(h), 1);
+      mbar_init(bar_p(h), 128);
+    }
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -410,36 +484,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
-      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ);
+      // S_h = Q K_h^T and dP_h = dO V_h^T (M = 128 queries, N = 64 keys 64h.., K = D)
+      auto issue_s = [&](int s, int h) {
+        const uint32_t roff = uint32_t(h) * 64 * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 64 * h, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s) + roff, kk), kIdS,
+                  kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128 + 64 * h, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s) + roff, kk), kIdS,
+                  kk > 0 ? 1u : 0u);
+        umma_commit(bar_s(h));
+      };
+      // dQ += dS_h K_h (M = 128 queries, N = D, K = 64 keys); dS_h sits in dP's columns
+      auto issue_grad = [&](int s, int h, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          umma_ts(tmem + 256, tmem + 128 + 64 * h + kk * 8, desc_mnmajor<D>(st_k(s), 4 * h + kk), kIdTS,
+                  (first && kk == 0) ? 0u : 1u);
+      };
+      bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ) &&
+                mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaK);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
       for (int it = 0; it < n && ok; ++it) {
-        const int s = it % C::kStages;
-        if (!(ok = mbar_wait(bar_full(s), (it / C::kStages) & 1, abort_flag, p.err, kSiteMmaK))) break;
+        const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
+        const bool more = it + 1 < n;
+        if (!(ok = mbar_wait(bar_p(0), it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // S = Q K^T and dP = dO V^T (M = 128 queries, N = 128 keys, K = D)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s), kk), kIdSS, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s), kk), kIdSS, kk > 0 ? 1u : 0u);
-        umma_commit(bar_s);
-        if (!(ok = mbar_wait(bar_p, it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        issue_grad(s, 0, it == 0);
+        if (more) {
+          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaK))) break;
+          tc_fence_after();
+          issue_s(s2, 0);
+        }
+        if (!(ok = mbar_wait(bar_p(1), it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // dQ += dS K (M = 128 queries, N = D, K = 128 keys); dS sits over dP
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256, tmem + 128 + kk * 8, desc_mnmajor<D>(st_k(s), kk), kIdTS,
-                  (it > 0 || kk > 0) ? 1u : 0u);
+        issue_grad(s, 1, false);
         umma_commit(bar_empty(s));
+        if (more) issue_s(s2, 1);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
     }
   } else {
-    // element-wise: one query row per thread
-    const int g = warp & 3;
+    // element-wise: one query row per thread, keys 64h .. 64h+63 of each tile
+    const int g = warp & 3, h = (warp - 2) >> 2;
     const int r = g * 32 + lane;
     const int qrow = itile * 128 + r;
     const uint32_t lane_off = uint32_t(g * 32) << 16;
@@ -448,39 +544,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float dr = p.drow[size_t(bh) * p.Lq_pad + qrow];
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(h), it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
       const int k0 = it * 128;
-      weights_row<false>(
-          tS, tdP, p.scale_log2,
+      weights_half<false>(
+          tS, tdP, p.scale_log2, h,
           [&](int e) { return k0 + e < p.Lk && (!p.causal || k0 + e <= qrow); },
           [&](int, float& l2_, float& dr_) {
             l2_ = l2;
             dr_ = dr;
           });
       tc_fence_before();
-      mbar_arrive(bar_p);
+      mbar_arrive(bar_p(h));
     }
-    // epilogue: scale * dQ row (warp-collective TMEM loads, predicated stores)
+    // epilogue: scale * dQ, columns [h D/2, (h+1) D/2) of this query's row
+    // (warp-collective TMEM loads, predicated stores)
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag, p.err, kSiteSoftmaxO));
     if (ok) {
       tc_fence_after();
       const bool valid = qrow < p.Lq;
       const size_t orow = (size_t(bh) * p.Lq + (valid ? qrow : 0)) * D;
 #pragma unroll 1
-      for (int cc = 0; cc < D; cc += 32) {
+      for (int cc = h * D / 2; cc < (h + 1) * D / 2; cc += 32) {
         float v[32];
         tmem_ld32_sync(tmem + lane_off + 256 + cc, v);
-        uint4* d4 = reinterpret_cast<uint4*>(p.out_a + orow + cc);
-        if (valid) {
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8)
-            d4[q8] = make_uint4(pack_bf16x2(v[8 * q8] * p.scale, v[8 * q8 + 1] * p.scale),
-                                pack_bf16x2(v[8 * q8 + 2] * p.scale, v[8 * q8 + 3] * p.scale),
-                                pack_bf16x2(v[8 * q8 + 4] * p.scale, v[8 * q8 + 5] * p.scale),
-                                pack_bf16x2(v[8 * q8 + 6] * p.scale, v[8 * q8 + 7] * p.scale));
-        }
+        if (valid) store_row32(p.out_a + orow + cc, v, p.scale);
       }
     }
   }
