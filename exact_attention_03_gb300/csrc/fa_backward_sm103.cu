@@ -24,17 +24,20 @@
 // results.  TMEM (512 columns): dK/dV kernel S^T [0,128) dP^T [128,256)
 // dV [256,256+D) dK [256+D,256+2D); dQ kernel S [0,128) dP [128,256)
 // dQ [256,256+D).
-// Each tile's 128 columns (queries in dK/dV, keys in dQ) are taken in two
-// halves of 64 with their own products, barriers and warp group, so that the
-// tensor core computes one half while the element-wise work of the other runs:
-//   S_0 dP_0 S_1 dP_1 | G_0 S'_0 dP'_0 G_1 S'_1 dP'_1 | G'_0 ...
-// (G_h = the gradient products that consume half h; ' = the next tile).  Half
-// h's bf16 results are packed into columns [64h, 64h+32) of the S and dP
-// regions, inside the columns that half itself consumed, and the next tile's
-// S_h is issued after G_h: tcgen05.mma operations from one thread execute in
-// order.  Warps: 0 = TMA producer, 1 = TMEM allocation + MMA issue, 2-5 = half
-// 0 and 6-9 = half 1 of the element-wise work and the epilogue (TMEM lane
-// quarter = warp % 4), so each SM sub-partition runs two element-wise warps.
+// The element-wise work runs in two phases per tile, each hidden behind two
+// products of the tensor core: P from S while dP is computed, dS from dP while
+// the first gradient product runs.  Issue order of the MMA thread:
+//   dK/dV:  S dP | dV S' dK dP' | dV' S'' dK' dP'' | ...
+//   dQ:     S dP | S' dQ dP' | S'' dQ' dP'' | ...
+// (' = the next tile; dV waits for P, dK and dQ for dS, the dQ kernel's S'
+// for the element-wise warps to have read S).  The next tile's S (dP) is
+// issued after the product that reads the bf16 data packed over S (dP):
+// tcgen05.mma operations from one thread execute in order.  Each row's 128
+// columns are split between two warps: warps 2-5 take columns 0-63 and warps
+// 6-9 columns 64-127 (TMEM lane quarter = warp % 4), so each SM sub-partition
+// runs two element-wise warps; half h's bf16 results are packed into columns
+// [64h, 64h+32) of the S and dP regions, inside the columns it consumed.
+// Warp 0 = TMA producer, warp 1 = TMEM allocation + MMA issue.
 // Every wait is bounded (the same routine as the forward kernels).
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -138,69 +141,58 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
   return sdesc_at(kDesc, tile + kk * 16 * 128);
 }
 
-// 32 columns at each of two TMEM addresses, with one wait for both loads
-__device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t tb, float (&a)[32], float (&b)[32]) {
-  uint32_t ra[32], rb[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]),
-        "=r"(ra[7]), "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]),
-        "=r"(ra[14]), "=r"(ra[15]), "=r"(ra[16]), "=r"(ra[17]), "=r"(ra[18]), "=r"(ra[19]),
-        "=r"(ra[20]), "=r"(ra[21]), "=r"(ra[22]), "=r"(ra[23]), "=r"(ra[24]), "=r"(ra[25]),
-        "=r"(ra[26]), "=r"(ra[27]), "=r"(ra[28]), "=r"(ra[29]), "=r"(ra[30]), "=r"(ra[31]),
-        "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]),
-        "=r"(rb[7]), "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]),
-        "=r"(rb[14]), "=r"(rb[15]), "=r"(rb[16]), "=r"(rb[17]), "=r"(rb[18]), "=r"(rb[19]),
-        "=r"(rb[20]), "=r"(rb[21]), "=r"(rb[22]), "=r"(rb[23]), "=r"(rb[24]), "=r"(rb[25]),
-        "=r"(rb[26]), "=r"(rb[27]), "=r"(rb[28]), "=r"(rb[29]), "=r"(rb[30]), "=r"(rb[31])
-      : "r"(ta), "r"(tb)
-      : "memory");
+// TMEM column of the bf16 operand for K-step kk (16 rows of the K dimension) of
+// a gradient product: half kk/4's data sits at [64 (kk/4), 64 (kk/4) + 32)
+__device__ __forceinline__ uint32_t packed_col(int kk) { return uint32_t(64 * (kk >> 2) + 8 * (kk & 3)); }
+
+// phase 1 of the element-wise step on half h of one 128-wide TMEM row: the
+// 64 scores of columns 64h .. 64h+63 (loaded from S into pv) become the
+// weights p = 2^(c s - lse2).  `l2(i)` gives column 64h+i's log2-domain LSE;
+// with MASK, `valid(i)` gives its mask and a masked column's exponent argument
+// becomes -inf (a select, not a branch around the exponential).
+template <bool MASK, class L2, class Valid>
+__device__ __forceinline__ void weights_p(float (&pv)[64], float c, L2 l2, Valid valid) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    a[i] = __uint_as_float(ra[i]);
-    b[i] = __uint_as_float(rb[i]);
+  for (int i = 0; i < 64; ++i) {
+    const float x = fmaf(pv[i], c, -l2(i));
+    pv[i] = ex2_approx(!MASK || valid(i) ? x : -INFINITY);
   }
 }
 
-// element-wise step on half h (columns 64h .. 64h+63) of one 128-wide row held
-// in TMEM (S^T/dP^T rows of keys, or S/dP rows of queries), in two chunks of 32
-// columns; the weights p and dS = p (dP - Dr) are packed to bf16 and written
-// back into the half's own consumed columns: chunk c of the half goes to
-// [64h + 16c, 64h + 16c + 16) of the S and dP regions.  `valid(e)` and
-// `coef(e, lse2, dr)` give the mask and the per-column terms of column e.
-template <bool WRITE_P, class Valid, class Coef>
-__device__ __forceinline__ void weights_half(uint32_t tS, uint32_t tdP, float c, int h, Valid valid, Coef coef) {
-#pragma unroll 1
+// bf16 pairs of 64 values into 32 TMEM columns at taddr
+__device__ __forceinline__ void store_packed64(uint32_t taddr, const float (&v)[64]) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  tmem_st32(taddr, w);
+}
+
+// phase 2: dS = p (dP - Dr) for the same 64 columns, dP read from tdP, packed
+// to bf16 into [64h, 64h+32) of the dP region.  `dr(i)` gives column
+// 64h+i's Dr (the dK/dV kernel) or the row's (the dQ kernel).
+template <class Dr>
+__device__ __forceinline__ void weights_ds(uint32_t tdP, int h, const float (&pv)[64], Dr dr) {
+#pragma unroll
   for (int ch = 0; ch < 2; ++ch) {
-    const int col = 64 * h + 32 * ch;
-    float s[32], dp[32];
-    tmem_ld32x2_sync(tS + col, tdP + col, s, dp);
-    uint32_t wp[16], wd[16];
+    float dp[32];
+    tmem_ld32_sync(tdP + 64 * h + 32 * ch, dp);
+    uint32_t w[16];
 #pragma unroll
-    for (int e2 = 0; e2 < 16; ++e2) {
-      float pv[2], dv[2];
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int e = col + 2 * e2 + k;
-        float l2, dr;
-        coef(e, l2, dr);
-        const float p = valid(e) ? ex2_approx(fmaf(s[2 * e2 + k], c, -l2)) : 0.f;
-        pv[k] = p;
-        dv[k] = p * (dp[2 * e2 + k] - dr);
-      }
-      wp[e2] = pack_bf16x2(pv[0], pv[1]);
-      wd[e2] = pack_bf16x2(dv[0], dv[1]);
+    for (int i = 0; i < 16; ++i) {
+      const int e = 32 * ch + 2 * i;
+      w[i] = pack_bf16x2(pv[e] * (dp[2 * i] - dr(e)), pv[e + 1] * (dp[2 * i + 1] - dr(e + 1)));
     }
-    if (WRITE_P) tmem_st16(tS + 64 * h + 16 * ch, wp);
-    tmem_st16(tdP + 64 * h + 16 * ch, wd);
+    tmem_st16(tdP + 64 * h + 16 * ch, w);
   }
+}
+
+// signal an mbarrier with one arrival per warp once the warp's TMEM stores
+// have completed
+__device__ __forceinline__ void warp_arrive_after_st(uint32_t bar, int lane) {
   tmem_st_wait();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
 }
 
 // bf16 store of 32 fp32 values times `mul` to 16-byte aligned global memory
@@ -233,9 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sBar = base + C::kBarOff;
   auto bar_full = [&](int s) { return sBar + 8 * s; };
   auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
-  const uint32_t bar_kv = sBar + 128, bar_done = sBar + 168;
-  auto bar_s = [&](int h) { return sBar + 136 + 8 * h; };
-  auto bar_p = [&](int h) { return sBar + 152 + 8 * h; };
+  const uint32_t bar_kv = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_P = sBar + 152,
+                 bar_dS = sBar + 160, bar_done = sBar + 168;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
@@ -252,10 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_kv, 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar_s(h), 1);
-      mbar_init(bar_p(h), 128);
-    }
+    mbar_init(bar_S, 1);
+    mbar_init(bar_dP, 1);
+    mbar_init(bar_P, 8);    // one arrival per element-wise warp
+    mbar_init(bar_dS, 8);
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -294,57 +285,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
-      // S^T_h = K Q_h^T and dP^T_h = V dO_h^T (M = 128 keys, N = 64 queries
-      // 64h.., K = D); rows 64h.. of a tile start 64 x 128 bytes into each of
-      // its 64-column blocks
-      auto issue_s = [&](int s, int h) {
-        const uint32_t roff = uint32_t(h) * 64 * 128;
+      // S^T = K Q^T, dP^T = V dO^T (M = 128 keys, N = 128 queries, K = D)
+      auto issue_s = [&](int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 64 * h, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s) + roff, kk), kIdS,
-                  kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128 + 64 * h, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s) + roff, kk), kIdS,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar_s(h));
+          umma_ss(tmem, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_S);
       };
-      // dV += P^T_h dO_h and dK += dS^T_h Q_h (M = 128 keys, N = D, K = 64 queries)
-      auto issue_grad = [&](int s, int h, bool first) {
+      auto issue_dp = [&](int s) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem + 256, tmem + 64 * h + kk * 8, desc_mnmajor<D>(st_do(s), 4 * h + kk), kIdTS,
-                  (first && kk == 0) ? 0u : 1u);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem + 256 + D, tmem + 128 + 64 * h + kk * 8, desc_mnmajor<D>(st_q(s), 4 * h + kk),
-                  kIdTS, (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_dP);
       };
       bool ok = mbar_wait(bar_kv, 0, abort_flag, p.err, kSiteMmaK) &&
                 mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaQ);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_s(0);
+        issue_dp(0);
       }
       for (int it = 0; it < n && ok; ++it) {
         const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
         const bool more = it + 1 < n;
-        if (!(ok = mbar_wait(bar_p(0), it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        if (!(ok = mbar_wait(bar_P, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        issue_grad(s, 0, it == 0);
+        // dV += P^T dO (M = 128 keys, N = D, K = 128 queries)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256, tmem + packed_col(kk), desc_mnmajor<D>(st_do(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
         if (more) {
           if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaQ))) break;
           tc_fence_after();
-          issue_s(s2, 0);
+          issue_s(s2);
         }
-        if (!(ok = mbar_wait(bar_p(1), it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        if (!(ok = mbar_wait(bar_dS, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        issue_grad(s, 1, false);
+        // dK += dS^T Q (M = 128 keys, N = D, K = 128 queries)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256 + D, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_q(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar_empty(s));
-        if (more) issue_s(s2, 1);
+        if (more) issue_dp(s2);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
@@ -356,31 +342,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = jt * 128 + r;
     const uint32_t lane_off = uint32_t(g * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
+    const bool key_ok = key < p.Lk;
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(h), it & 1, abort_flag, p.err, kSiteSoftmaxS));
-      if (!ok) break;
-      tc_fence_after();
-      const int q0 = (i0 + it) * 128;
-      const bool key_ok = key < p.Lk;
+      const int q0 = (i0 + it) * 128 + 64 * h;
       const bool diag = p.causal && (i0 + it) == jt;
       // the stage's LSE2 / Dr slices landed with its Q, dO tiles: wait on that
-      // barrier too (already complete; it cannot move on before both groups
-      // release the stage) so that the copied values are visible here
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_full(it % C::kStages), (it / C::kStages) & 1,
-                                             abort_flag, p.err, kSiteSoftmaxS));
+      // barrier too (already complete; it cannot move on before this tile's
+      // products are done) so that the copied values are visible here
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_S, it & 1, abort_flag, p.err, kSiteSoftmaxS) &&
+                                       mbar_wait(bar_full(it % C::kStages), (it / C::kStages) & 1,
+                                                 abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
-      const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStages) - base));
+      tc_fence_after();
+      const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStages) - base)) + 64 * h;
       const float* vdr = vl2 + 128;
-      weights_half<true>(
-          tS, tdP, p.scale_log2, h,
-          [&](int e) { return key_ok && (!diag || key <= q0 + e); },
-          [&](int e, float& l2, float& dr) {
-            l2 = vl2[e];
-            dr = vdr[e];
-          });
-      tc_fence_before();
-      mbar_arrive(bar_p(h));
+      float pv[64];
+      // masked entries: keys past Lk (last key tile) and the causal diagonal
+      // tile; query rows past Lq carry LSE2 = +inf and come out 0 either way
+      auto l2 = [&](int i) { return vl2[i]; };
+      auto valid = [&](int i) { return key_ok && (!diag || key <= q0 + i); };
+      tmem_ld64_sync(tS + 64 * h, pv);
+      if (__all_sync(0xffffffffu, key_ok && !diag))
+        weights_p<false>(pv, p.scale_log2, l2, valid);
+      else
+        weights_p<true>(pv, p.scale_log2, l2, valid);
+      store_packed64(tS + 64 * h, pv);
+      warp_arrive_after_st(bar_P, lane);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dP, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      tc_fence_after();
+      weights_ds(tdP, h, pv, [&](int i) { return vdr[i]; });
+      warp_arrive_after_st(bar_dS, lane);
     }
     // epilogue: group 0 writes the dV row of this key, group 1 scale * dK.
     // The TMEM loads are warp-collective: every lane takes part, only the
@@ -426,9 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sBar = base + C::kBarOff;
   auto bar_full = [&](int s) { return sBar + 8 * s; };
   auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
-  const uint32_t bar_q = sBar + 128, bar_done = sBar + 168;
-  auto bar_s = [&](int h) { return sBar + 136 + 8 * h; };
-  auto bar_p = [&](int h) { return sBar + 152 + 8 * h; };
+  const uint32_t bar_q = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_Sfree = sBar + 152,
+                 bar_dS = sBar + 160, bar_done = sBar + 168;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
@@ -445,10 +437,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_q, 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(bar_s(h), 1);
-      mbar_init(bar_p(h), 128);
-    }
+    mbar_init(bar_S, 1);
+    mbar_init(bar_dP, 1);
+    mbar_init(bar_Sfree, 8);   // one arrival per element-wise warp
+    mbar_init(bar_dS, 8);
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -484,51 +476,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
-      // S_h = Q K_h^T and dP_h = dO V_h^T (M = 128 queries, N = 64 keys 64h.., K = D)
-      auto issue_s = [&](int s, int h) {
-        const uint32_t roff = uint32_t(h) * 64 * 128;
+      // S = Q K^T, dP = dO V^T (M = 128 queries, N = 128 keys, K = D)
+      auto issue_s = [&](int s) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 64 * h, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s) + roff, kk), kIdS,
-                  kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128 + 64 * h, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s) + roff, kk), kIdS,
-                  kk > 0 ? 1u : 0u);
-        umma_commit(bar_s(h));
+          umma_ss(tmem, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_S);
       };
-      // dQ += dS_h K_h (M = 128 queries, N = D, K = 64 keys); dS_h sits in dP's columns
-      auto issue_grad = [&](int s, int h, bool first) {
+      auto issue_dp = [&](int s) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem + 256, tmem + 128 + 64 * h + kk * 8, desc_mnmajor<D>(st_k(s), 4 * h + kk), kIdTS,
-                  (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          umma_ss(tmem + 128, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+        umma_commit(bar_dP);
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ) &&
                 mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaK);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_s(0);
+        issue_dp(0);
       }
       for (int it = 0; it < n && ok; ++it) {
         const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
         const bool more = it + 1 < n;
-        if (!(ok = mbar_wait(bar_p(0), it & 1, abort_flag, p.err, kSiteMmaP))) break;
-        tc_fence_after();
-        issue_grad(s, 0, it == 0);
         if (more) {
-          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaK))) break;
+          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaK) &&
+                     mbar_wait(bar_Sfree, it & 1, abort_flag, p.err, kSiteMmaP)))
+            break;
           tc_fence_after();
-          issue_s(s2, 0);
+          issue_s(s2);
         }
-        if (!(ok = mbar_wait(bar_p(1), it & 1, abort_flag, p.err, kSiteMmaP))) break;
+        if (!(ok = mbar_wait(bar_dS, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        issue_grad(s, 1, false);
+        // dQ += dS K (M = 128 queries, N = D, K = 128 keys); dS sits in dP's columns
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ts(tmem + 256, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_k(s), kk), kIdTS,
+                  (it > 0 || kk > 0) ? 1u : 0u);
         umma_commit(bar_empty(s));
-        if (more) issue_s(s2, 1);
+        if (more) issue_dp(s2);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
@@ -544,19 +532,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float dr = p.drow[size_t(bh) * p.Lq_pad + qrow];
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s(h), it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_S, it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
-      const int k0 = it * 128;
-      weights_half<false>(
-          tS, tdP, p.scale_log2, h,
-          [&](int e) { return k0 + e < p.Lk && (!p.causal || k0 + e <= qrow); },
-          [&](int, float& l2_, float& dr_) {
-            l2_ = l2;
-            dr_ = dr;
-          });
+      const int k0 = it * 128 + 64 * h;
+      float pv[64];
+      // masked entries: keys past Lk (last key tile) and keys above the
+      // causal diagonal; the whole tile is checked once (uniform for the CTA)
+      auto l2f = [&](int) { return l2; };
+      auto valid = [&](int i) { return k0 + i < p.Lk && (!p.causal || k0 + i <= qrow); };
+      tmem_ld64_sync(tS + 64 * h, pv);
+      // S is in registers: the next tile's S may overwrite it
       tc_fence_before();
-      mbar_arrive(bar_p(h));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_Sfree);
+      if (it * 128 + 128 <= p.Lk && (!p.causal || it * 128 + 127 <= itile * 128))
+        weights_p<false>(pv, p.scale_log2, l2f, valid);
+      else
+        weights_p<true>(pv, p.scale_log2, l2f, valid);
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_dP, it & 1, abort_flag, p.err, kSiteSoftmaxS));
+      if (!ok) break;
+      tc_fence_after();
+      weights_ds(tdP, h, pv, [&](int) { return dr; });
+      warp_arrive_after_st(bar_dS, lane);
     }
     // epilogue: scale * dQ, columns [h D/2, (h+1) D/2) of this query's row
     // (warp-collective TMEM loads, predicated stores)
