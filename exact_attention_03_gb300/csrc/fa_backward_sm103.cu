@@ -37,7 +37,10 @@
 // 6-9 columns 64-127 (TMEM lane quarter = warp % 4), so each SM sub-partition
 // runs two element-wise warps; half h's bf16 results are packed into columns
 // [64h, 64h+32) of the S and dP regions, inside the columns it consumed.
-// Warp 0 = TMA producer, warp 1 = TMEM allocation + MMA issue.
+// Warp 0 = TMA producer of the fixed tiles' first and ring A (Q tiles with
+// their LSE2 / Dr slices in dK/dV, K tiles in dQ), warp 10 = TMA producer of
+// the fixed tiles' second and ring B (dO or V tiles): two issuing threads
+// double the TMA rate.  Warp 1 = TMEM allocation + MMA issue.
 // Every wait is bounded (the same routine as the forward kernels).
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
@@ -47,19 +50,23 @@
 namespace fa {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;   // 11 warps
 constexpr float kLog2e = 1.44269504088896340736f;
 
-template <int D>
+template <int D, bool DQ>
 struct BwCfg {
   static constexpr int kTileBytes = 128 * D * 2;        // one 128-row tile (one TMA box)
   static constexpr int kSubBytes = 128 * 128;           // one 64-column block of a tile
-  static constexpr int kStages = D == 64 ? 4 : 2;       // ring of (two-tile) stages
+  // ring A: Q tiles (dK/dV kernel) or K tiles (dQ kernel); ring B: dO or V tiles
+  static constexpr int kStagesA = D == 64 ? 4 : (DQ ? 3 : 2);
+  static constexpr int kStagesB = D == 64 ? 4 : 2;
   static constexpr int kFixedOff = 0;                   // the CTA's own two tiles
-  static constexpr int kRingOff = 2 * kTileBytes;       // stage s: tiles at +2s, +2s+1
-  static constexpr int kVecOff = kRingOff + kStages * 2 * kTileBytes;  // per stage: 128 LSE2 + 128 Dr
-  static constexpr int kBarOff = kVecOff + kStages * 1024;
+  static constexpr int kRingAOff = 2 * kTileBytes;
+  static constexpr int kRingBOff = kRingAOff + kStagesA * kTileBytes;
+  static constexpr int kVecOff = kRingBOff + kStagesB * kTileBytes;  // dK/dV: per A stage 128 LSE2 + 128 Dr
+  static constexpr int kBarOff = kVecOff + (DQ ? 0 : kStagesA * 1024);
   static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
 struct BwParams {
@@ -85,6 +92,14 @@ __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
   for (uint32_t it = 0; it < (1u << 22); ++it) {
     if (mbar_try_wait(bar, parity)) return;
     if ((it & 15u) == 15u && globaltimer_ns() - t0 > 50000000ull) return;  // 50 ms
+  }
+}
+
+// before exit: wait (bounded) for the last copies into each used stage of a ring
+__device__ __forceinline__ void drain_ring(uint32_t full0, int stages, int issued) {
+  for (int s = 0; s < stages && s < issued; ++s) {
+    const int last = s + stages * ((issued - 1 - s) / stages);
+    drain(full0 + 8 * s, (last / stages) & 1);
   }
 }
 
@@ -133,11 +148,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* o
 template <int D>
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
   constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);
-  return sdesc_at(kDesc, tile + (kk >> 2) * BwCfg<D>::kSubBytes + (kk & 3) * 32);
+  return sdesc_at(kDesc, tile + (kk >> 2) * BwCfg<D, false>::kSubBytes + (kk & 3) * 32);
 }
 template <int D>
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
-  constexpr uint64_t kDesc = sdesc_sw128(0, BwCfg<D>::kSubBytes, 1024);
+  constexpr uint64_t kDesc = sdesc_sw128(0, BwCfg<D, false>::kSubBytes, 1024);
   return sdesc_at(kDesc, tile + kk * 16 * 128);
 }
 
@@ -213,18 +228,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwParams p) {
-  using C = BwCfg<D>;
+  using C = BwCfg<D, false>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sK = base + C::kFixedOff, sV = sK + C::kTileBytes;
-  auto st_q = [&](int s) { return base + C::kRingOff + (2 * s) * C::kTileBytes; };
-  auto st_do = [&](int s) { return base + C::kRingOff + (2 * s + 1) * C::kTileBytes; };
+  auto st_q = [&](int s) { return base + C::kRingAOff + s * C::kTileBytes; };
+  auto st_do = [&](int s) { return base + C::kRingBOff + s * C::kTileBytes; };
   auto st_vec = [&](int s) { return base + C::kVecOff + s * 1024; };
   const uint32_t sBar = base + C::kBarOff;
-  auto bar_full = [&](int s) { return sBar + 8 * s; };
-  auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
+  auto full_a = [&](int s) { return sBar + 8 * s; };
+  auto full_b = [&](int s) { return sBar + 32 + 8 * s; };
+  auto empty_a = [&](int s) { return sBar + 64 + 8 * s; };
+  auto empty_b = [&](int s) { return sBar + 96 + 8 * s; };
   const uint32_t bar_kv = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_P = sBar + 152,
                  bar_dS = sBar + 160, bar_done = sBar + 168;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
@@ -238,11 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = nq_all - i0;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_a(s), 1);
+      mbar_init(empty_b(s), 1);
     }
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_kv, 2);   // one arrival (with its bytes) from each producer
     mbar_init(bar_S, 1);
     mbar_init(bar_dP, 1);
     mbar_init(bar_P, 8);    // one arrival per element-wise warp
@@ -260,77 +279,87 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 10) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_kv, 2 * C::kTileBytes);
-      tma_load_tile(sK, &tmK, bar_kv, jt * 128, bh);
-      tma_load_tile(sV, &tmV, bar_kv, jt * 128, bh);
+      const bool ra = warp == 0;
+      const int stages = ra ? C::kStagesA : C::kStagesB;
+      mbar_arrive_expect_tx(bar_kv, C::kTileBytes);
+      tma_load_tile(ra ? sK : sV, ra ? &tmK : &tmV, bar_kv, jt * 128, bh);
       int issued = 0;
       for (int it = 0; it < n; ++it) {
-        const int s = it % C::kStages, use = it / C::kStages;
-        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
-        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes + 1024);
-        tma_load_tile(st_q(s), &tmQ, bar_full(s), (i0 + it) * 128, bh);
-        tma_load_tile(st_do(s), &tmDO, bar_full(s), (i0 + it) * 128, bh);
-        const size_t voff = size_t(bh) * p.Lq_pad + size_t(i0 + it) * 128;
-        bulk_load(st_vec(s), p.lse2 + voff, 512, bar_full(s));
-        bulk_load(st_vec(s) + 512, p.drow + voff, 512, bar_full(s));
+        const int s = it % stages, use = it / stages;
+        if (!mbar_wait(ra ? empty_a(s) : empty_b(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty))
+          break;
+        if (ra) {
+          mbar_arrive_expect_tx(full_a(s), C::kTileBytes + 1024);
+          tma_load_tile(st_q(s), &tmQ, full_a(s), (i0 + it) * 128, bh);
+          const size_t voff = size_t(bh) * p.Lq_pad + size_t(i0 + it) * 128;
+          bulk_load(st_vec(s), p.lse2 + voff, 512, full_a(s));
+          bulk_load(st_vec(s) + 512, p.drow + voff, 512, full_a(s));
+        } else {
+          mbar_arrive_expect_tx(full_b(s), C::kTileBytes);
+          tma_load_tile(st_do(s), &tmDO, full_b(s), (i0 + it) * 128, bh);
+        }
         ++issued;
       }
       drain(bar_kv, 0);
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
-        drain(bar_full(s), (last / C::kStages) & 1);
-      }
+      drain_ring(ra ? full_a(0) : full_b(0), stages, issued);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
       // S^T = K Q^T, dP^T = V dO^T (M = 128 keys, N = 128 queries, K = D)
-      auto issue_s = [&](int s) {
+      auto issue_s = [&](int sa) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem, desc_kmajor<D>(sK, kk), desc_kmajor<D>(st_q(sa), kk), kIdSS, kk > 0 ? 1u : 0u);
         umma_commit(bar_S);
       };
-      auto issue_dp = [&](int s) {
+      auto issue_dp = [&](int sb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + 128, desc_kmajor<D>(sV, kk), desc_kmajor<D>(st_do(sb), kk), kIdSS, kk > 0 ? 1u : 0u);
         umma_commit(bar_dP);
       };
       bool ok = mbar_wait(bar_kv, 0, abort_flag, p.err, kSiteMmaK) &&
-                mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaQ);
+                mbar_wait(full_a(0), 0, abort_flag, p.err, kSiteMmaQ) &&
+                mbar_wait(full_b(0), 0, abort_flag, p.err, kSiteMmaQ);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         issue_dp(0);
       }
       for (int it = 0; it < n && ok; ++it) {
-        const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
+        const int sa = it % C::kStagesA, sb = it % C::kStagesB;
+        const int sa2 = (it + 1) % C::kStagesA, sb2 = (it + 1) % C::kStagesB;
         const bool more = it + 1 < n;
+        // the next dO stage (released a phase earlier than Q's), while the
+        // element-wise warps still work on P
+        if (more && !(ok = mbar_wait(full_b(sb2), ((it + 1) / C::kStagesB) & 1, abort_flag, p.err, kSiteMmaQ)))
+          break;
         if (!(ok = mbar_wait(bar_P, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // dV += P^T dO (M = 128 keys, N = D, K = 128 queries)
+        // dV += P^T dO (M = 128 keys, N = D, K = 128 queries); the last use of dO
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256, tmem + packed_col(kk), desc_mnmajor<D>(st_do(s), kk), kIdTS,
+          umma_ts(tmem + 256, tmem + packed_col(kk), desc_mnmajor<D>(st_do(sb), kk), kIdTS,
                   (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(empty_b(sb));
         if (more) {
-          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaQ))) break;
+          if (!(ok = mbar_wait(full_a(sa2), ((it + 1) / C::kStagesA) & 1, abort_flag, p.err, kSiteMmaQ))) break;
           tc_fence_after();
-          issue_s(s2);
+          issue_s(sa2);
         }
         if (!(ok = mbar_wait(bar_dS, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // dK += dS^T Q (M = 128 keys, N = D, K = 128 queries)
+        // dK += dS^T Q (M = 128 keys, N = D, K = 128 queries); the last use of Q
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256 + D, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_q(s), kk), kIdTS,
+          umma_ts(tmem + 256 + D, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_q(sa), kk), kIdTS,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar_empty(s));
-        if (more) issue_dp(s2);
+        umma_commit(empty_a(sa));
+        if (more) issue_dp(sb2);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
@@ -351,11 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // barrier too (already complete; it cannot move on before this tile's
       // products are done) so that the copied values are visible here
       ok = __all_sync(0xffffffffu, mbar_wait(bar_S, it & 1, abort_flag, p.err, kSiteSoftmaxS) &&
-                                       mbar_wait(bar_full(it % C::kStages), (it / C::kStages) & 1,
+                                       mbar_wait(full_a(it % C::kStagesA), (it / C::kStagesA) & 1,
                                                  abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
-      const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStages) - base)) + 64 * h;
+      const float* vl2 = reinterpret_cast<const float*>(gbase + (st_vec(it % C::kStagesA) - base)) + 64 * h;
       const float* vdr = vl2 + 128;
       float pv[64];
       // masked entries: keys past Lk (last key tile) and the causal diagonal
@@ -408,17 +437,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwParams p) {
-  using C = BwCfg<D>;
+  using C = BwCfg<D, true>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base + C::kFixedOff, sDO = sQ + C::kTileBytes;
-  auto st_k = [&](int s) { return base + C::kRingOff + (2 * s) * C::kTileBytes; };
-  auto st_v = [&](int s) { return base + C::kRingOff + (2 * s + 1) * C::kTileBytes; };
+  auto st_k = [&](int s) { return base + C::kRingAOff + s * C::kTileBytes; };
+  auto st_v = [&](int s) { return base + C::kRingBOff + s * C::kTileBytes; };
   const uint32_t sBar = base + C::kBarOff;
-  auto bar_full = [&](int s) { return sBar + 8 * s; };
-  auto bar_empty = [&](int s) { return sBar + 64 + 8 * s; };
+  auto full_a = [&](int s) { return sBar + 8 * s; };
+  auto full_b = [&](int s) { return sBar + 32 + 8 * s; };
+  auto empty_a = [&](int s) { return sBar + 64 + 8 * s; };
+  auto empty_b = [&](int s) { return sBar + 96 + 8 * s; };
   const uint32_t bar_q = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_Sfree = sBar + 152,
                  bar_dS = sBar + 160, bar_done = sBar + 168;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
@@ -432,11 +463,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n = p.causal ? min(nk_all, itile + 1) : nk_all;   // causal: keys <= query
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_a(s), 1);
+      mbar_init(empty_b(s), 1);
     }
-    mbar_init(bar_q, 1);
+    mbar_init(bar_q, 2);       // one arrival (with its bytes) from each producer
     mbar_init(bar_S, 1);
     mbar_init(bar_dP, 1);
     mbar_init(bar_Sfree, 8);   // one arrival per element-wise warp
@@ -454,69 +487,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 10) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, 2 * C::kTileBytes);
-      tma_load_tile(sQ, &tmQ, bar_q, itile * 128, bh);
-      tma_load_tile(sDO, &tmDO, bar_q, itile * 128, bh);
+      const bool ra = warp == 0;
+      const int stages = ra ? C::kStagesA : C::kStagesB;
+      mbar_arrive_expect_tx(bar_q, C::kTileBytes);
+      tma_load_tile(ra ? sQ : sDO, ra ? &tmQ : &tmDO, bar_q, itile * 128, bh);
       int issued = 0;
       for (int it = 0; it < n; ++it) {
-        const int s = it % C::kStages, use = it / C::kStages;
-        if (!mbar_wait(bar_empty(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty)) break;
-        mbar_arrive_expect_tx(bar_full(s), 2 * C::kTileBytes);
-        tma_load_tile(st_k(s), &tmK, bar_full(s), it * 128, bh);
-        tma_load_tile(st_v(s), &tmV, bar_full(s), it * 128, bh);
+        const int s = it % stages, use = it / stages;
+        const uint32_t full = ra ? full_a(s) : full_b(s);
+        if (!mbar_wait(ra ? empty_a(s) : empty_b(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty))
+          break;
+        mbar_arrive_expect_tx(full, C::kTileBytes);
+        tma_load_tile(ra ? st_k(s) : st_v(s), ra ? &tmK : &tmV, full, it * 128, bh);
         ++issued;
       }
       drain(bar_q, 0);
-      for (int s = 0; s < C::kStages && s < issued; ++s) {
-        const int last = s + C::kStages * ((issued - 1 - s) / C::kStages);
-        drain(bar_full(s), (last / C::kStages) & 1);
-      }
+      drain_ring(ra ? full_a(0) : full_b(0), stages, issued);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t kIdSS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdTS = idesc_bf16_f32(128, D, false, true);
       // S = Q K^T, dP = dO V^T (M = 128 queries, N = 128 keys, K = D)
-      auto issue_s = [&](int s) {
+      auto issue_s = [&](int sa) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem, desc_kmajor<D>(sQ, kk), desc_kmajor<D>(st_k(sa), kk), kIdSS, kk > 0 ? 1u : 0u);
         umma_commit(bar_S);
       };
-      auto issue_dp = [&](int s) {
+      // dP's commit also releases its V stage (V has no other use)
+      auto issue_dp = [&](int sb) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          umma_ss(tmem + 128, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(s), kk), kIdSS, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + 128, desc_kmajor<D>(sDO, kk), desc_kmajor<D>(st_v(sb), kk), kIdSS, kk > 0 ? 1u : 0u);
         umma_commit(bar_dP);
+        umma_commit(empty_b(sb));
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ) &&
-                mbar_wait(bar_full(0), 0, abort_flag, p.err, kSiteMmaK);
+                mbar_wait(full_a(0), 0, abort_flag, p.err, kSiteMmaK) &&
+                mbar_wait(full_b(0), 0, abort_flag, p.err, kSiteMmaK);
       if (ok) {
         tc_fence_after();
         issue_s(0);
         issue_dp(0);
       }
       for (int it = 0; it < n && ok; ++it) {
-        const int s = it % C::kStages, s2 = (it + 1) % C::kStages;
+        const int sa = it % C::kStagesA;
+        const int sa2 = (it + 1) % C::kStagesA, sb2 = (it + 1) % C::kStagesB;
         const bool more = it + 1 < n;
         if (more) {
-          if (!(ok = mbar_wait(bar_full(s2), ((it + 1) / C::kStages) & 1, abort_flag, p.err, kSiteMmaK) &&
+          if (!(ok = mbar_wait(full_a(sa2), ((it + 1) / C::kStagesA) & 1, abort_flag, p.err, kSiteMmaK) &&
+                     mbar_wait(full_b(sb2), ((it + 1) / C::kStagesB) & 1, abort_flag, p.err, kSiteMmaK) &&
                      mbar_wait(bar_Sfree, it & 1, abort_flag, p.err, kSiteMmaP)))
             break;
           tc_fence_after();
-          issue_s(s2);
+          issue_s(sa2);
         }
         if (!(ok = mbar_wait(bar_dS, it & 1, abort_flag, p.err, kSiteMmaP))) break;
         tc_fence_after();
-        // dQ += dS K (M = 128 queries, N = D, K = 128 keys); dS sits in dP's columns
+        // dQ += dS K (M = 128 queries, N = D, K = 128 keys); dS sits in dP's
+        // columns; the last use of K
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + 256, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_k(s), kk), kIdTS,
+          umma_ts(tmem + 256, tmem + 128 + packed_col(kk), desc_mnmajor<D>(st_k(sa), kk), kIdTS,
                   (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar_empty(s));
-        if (more) issue_dp(s2);
+        umma_commit(empty_a(sa));
+        if (more) issue_dp(sb2);
       }
       umma_commit(bar_done);
       drain(bar_done, 0);
@@ -583,7 +621,8 @@ template <int D>
 int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, float scale,
                  int causal, float* ws, int* err, cudaStream_t stream) {
-  using C = BwCfg<D>;
+  using CK = BwCfg<D, false>;
+  using CQ = BwCfg<D, true>;
   CUtensorMap mq, mk, mv, mdo;
   int st = make_tensor_map_bf16(&mq, q, BH, Lq, D);
   if (st == 0) st = make_tensor_map_bf16(&mk, k, BH, Lk, D);
@@ -613,20 +652,20 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
     if (cudaGetLastError() != cudaSuccess) return -4;
   }
   if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess ||
+                           CK::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmemBytes) != cudaSuccess)
+                           CQ::kSmemBytes) != cudaSuccess)
     return -4;
   const long long nk = (long long)((Lk + 127) / 128) * BH;
   const long long nq = (long long)((Lq + 127) / 128) * BH;
   if (nk > 0x7fffffffLL || nq > 0x7fffffffLL) return -2;
   p.out_a = static_cast<__nv_bfloat16*>(dk);
   p.out_b = static_cast<__nv_bfloat16*>(dv);
-  fa_bwd_dkdv_kernel<D><<<dim3(unsigned(nk)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dkdv_kernel<D><<<dim3(unsigned(nk)), dim3(kThreads), CK::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return -4;
   p.out_a = static_cast<__nv_bfloat16*>(dq);
   p.out_b = nullptr;
-  fa_bwd_dq_kernel<D><<<dim3(unsigned(nq)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dq_kernel<D><<<dim3(unsigned(nq)), dim3(kThreads), CQ::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
