@@ -103,6 +103,33 @@ __device__ __forceinline__ void drain_ring(uint32_t full0, int stages, int issue
   }
 }
 
+// Grid order: heads in groups of kGroupHeads, all tiles of a group before the
+// next group, so that the CTAs resident at one time share a few heads' tiles
+// in L2 (a head's K and V at L = 8192, D = 128 are 4 MB) instead of streaming
+// every head's from HBM; within a group, rank 0 (the tile with the most work
+// when causal) of every head first, then rank 1, ...
+constexpr int kGroupHeads = 8;
+struct TileOrder {
+  int rank, bh;
+};
+__device__ __forceinline__ TileOrder tile_order(int block, int BH, int ntiles) {
+  const int full = BH / kGroupHeads * kGroupHeads;   // heads in whole groups
+  const long long in_full = (long long)full * ntiles;
+  TileOrder t;
+  if (block < in_full) {
+    const int grp = int(block / ((long long)kGroupHeads * ntiles));
+    const int idx = int(block - (long long)grp * kGroupHeads * ntiles);
+    t.rank = idx / kGroupHeads;
+    t.bh = grp * kGroupHeads + idx % kGroupHeads;
+  } else {
+    const int rest = BH - full;
+    const int idx = int(block - in_full);
+    t.rank = idx / rest;
+    t.bh = full + idx % rest;
+  }
+  return t;
+}
+
 // ---------------------------------------------------------------- preparation
 
 template <int D>
@@ -248,8 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int jt = int(blockIdx.x) / p.BH;      // key tile (the most query tiles first when causal)
-  const int bh = int(blockIdx.x) % p.BH;
+  const TileOrder to = tile_order(int(blockIdx.x), p.BH, (p.Lk + 127) / 128);
+  const int jt = to.rank;      // key tile (the most query tiles first when causal)
+  const int bh = to.bh;
   const int nq_all = (p.Lq + 127) / 128;
   const int i0 = p.causal ? jt : 0;           // causal: queries q >= key, so query tiles >= jt
   const int n = nq_all - i0;
@@ -446,33 +474,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_k = [&](int s) { return base + C::kRingAOff + s * C::kTileBytes; };
   auto st_v = [&](int s) { return base + C::kRingBOff + s * C::kTileBytes; };
   const uint32_t sBar = base + C::kBarOff;
-  auto full_a = [&](int s) { return sBar + 8 * s; };
-  auto full_b = [&](int s) { return sBar + 32 + 8 * s; };
+  // ready(j): K_j and V_j have landed and the element-wise warps have read
+  // S_(j-1) out of TMEM, so S_j may be computed (four slots by j mod 4)
+  auto ready = [&](int j) { return sBar + 8 * (j & 3); };
   auto empty_a = [&](int s) { return sBar + 64 + 8 * s; };
   auto empty_b = [&](int s) { return sBar + 96 + 8 * s; };
-  const uint32_t bar_q = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_Sfree = sBar + 152,
-                 bar_dS = sBar + 160, bar_done = sBar + 168;
+  const uint32_t bar_q = sBar + 128, bar_S = sBar + 136, bar_dP = sBar + 144, bar_dS = sBar + 160,
+                 bar_done = sBar + 168;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::kBarOff + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq_all = (p.Lq + 127) / 128;
-  const int itile = nq_all - 1 - int(blockIdx.x) / p.BH;  // the most key tiles first when causal
-  const int bh = int(blockIdx.x) % p.BH;
+  const TileOrder to = tile_order(int(blockIdx.x), p.BH, nq_all);
+  const int itile = nq_all - 1 - to.rank;  // the most key tiles first when causal
+  const int bh = to.bh;
   const int nk_all = (p.Lk + 127) / 128;
   const int n = p.causal ? min(nk_all, itile + 1) : nk_all;   // causal: keys <= query
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 4; ++s) {
-      mbar_init(full_a(s), 1);
-      mbar_init(full_b(s), 1);
+      mbar_init(ready(s), 2 + 8);   // each producer (with its bytes) + each element-wise warp
       mbar_init(empty_a(s), 1);
       mbar_init(empty_b(s), 1);
     }
     mbar_init(bar_q, 2);       // one arrival (with its bytes) from each producer
     mbar_init(bar_S, 1);
     mbar_init(bar_dP, 1);
-    mbar_init(bar_Sfree, 8);   // one arrival per element-wise warp
     mbar_init(bar_dS, 8);
     mbar_init(bar_done, 1);
     *abort_flag = 0;
@@ -494,17 +522,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar_q, C::kTileBytes);
       tma_load_tile(ra ? sQ : sDO, ra ? &tmQ : &tmDO, bar_q, itile * 128, bh);
       int issued = 0;
+      // no party runs four tiles ahead of the issuer's waits on ready(), so a
+      // slot's previous phase has completed before anyone arrives on it again
       for (int it = 0; it < n; ++it) {
         const int s = it % stages, use = it / stages;
-        const uint32_t full = ra ? full_a(s) : full_b(s);
         if (!mbar_wait(ra ? empty_a(s) : empty_b(s), (use & 1) ^ 1, abort_flag, p.err, kSiteProducerEmpty))
           break;
-        mbar_arrive_expect_tx(full, C::kTileBytes);
-        tma_load_tile(ra ? st_k(s) : st_v(s), ra ? &tmK : &tmV, full, it * 128, bh);
+        mbar_arrive_expect_tx(ready(it), C::kTileBytes);
+        tma_load_tile(ra ? st_k(s) : st_v(s), ra ? &tmK : &tmV, ready(it), it * 128, bh);
         ++issued;
       }
       drain(bar_q, 0);
-      drain_ring(ra ? full_a(0) : full_b(0), stages, issued);
+      for (int j = max(0, issued - 4); j < issued; ++j) drain(ready(j), (j >> 2) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -526,8 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(empty_b(sb));
       };
       bool ok = mbar_wait(bar_q, 0, abort_flag, p.err, kSiteMmaQ) &&
-                mbar_wait(full_a(0), 0, abort_flag, p.err, kSiteMmaK) &&
-                mbar_wait(full_b(0), 0, abort_flag, p.err, kSiteMmaK);
+                mbar_wait(ready(0), 0, abort_flag, p.err, kSiteMmaK);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -538,10 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sa2 = (it + 1) % C::kStagesA, sb2 = (it + 1) % C::kStagesB;
         const bool more = it + 1 < n;
         if (more) {
-          if (!(ok = mbar_wait(full_a(sa2), ((it + 1) / C::kStagesA) & 1, abort_flag, p.err, kSiteMmaK) &&
-                     mbar_wait(full_b(sb2), ((it + 1) / C::kStagesB) & 1, abort_flag, p.err, kSiteMmaK) &&
-                     mbar_wait(bar_Sfree, it & 1, abort_flag, p.err, kSiteMmaP)))
-            break;
+          if (!(ok = mbar_wait(ready(it + 1), ((it + 1) >> 2) & 1, abort_flag, p.err, kSiteMmaK))) break;
           tc_fence_after();
           issue_s(sa2);
         }
@@ -568,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
     const float l2 = p.lse2[size_t(bh) * p.Lq_pad + qrow];
     const float dr = p.drow[size_t(bh) * p.Lq_pad + qrow];
+    if (lane == 0) mbar_arrive(ready(0));   // nothing to read before the first tile
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_S, it & 1, abort_flag, p.err, kSiteSoftmaxS));
@@ -583,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S is in registers: the next tile's S may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_Sfree);
+      if (lane == 0) mbar_arrive(ready(it + 1));
       if (it * 128 + 128 <= p.Lk && (!p.causal || it * 128 + 127 <= itile * 128))
         weights_p<false>(pv, p.scale_log2, l2f, valid);
       else
