@@ -76,6 +76,7 @@ struct BwParams {
   const float* drow;      // [BH][Lq_pad]: rowsum(dO * O), 0 past Lq
   int* err;
   int BH, Lq, Lk, Lq_pad;
+  int group;              // heads per group of the grid order
   int causal;
   float scale, scale_log2;
 };
@@ -101,33 +102,6 @@ __device__ __forceinline__ void drain_ring(uint32_t full0, int stages, int issue
     const int last = s + stages * ((issued - 1 - s) / stages);
     drain(full0 + 8 * s, (last / stages) & 1);
   }
-}
-
-// Grid order: heads in groups of kGroupHeads, all tiles of a group before the
-// next group, so that the CTAs resident at one time share a few heads' tiles
-// in L2 (a head's K and V at L = 8192, D = 128 are 4 MB) instead of streaming
-// every head's from HBM; within a group, rank 0 (the tile with the most work
-// when causal) of every head first, then rank 1, ...
-constexpr int kGroupHeads = 8;
-struct TileOrder {
-  int rank, bh;
-};
-__device__ __forceinline__ TileOrder tile_order(int block, int BH, int ntiles) {
-  const int full = BH / kGroupHeads * kGroupHeads;   // heads in whole groups
-  const long long in_full = (long long)full * ntiles;
-  TileOrder t;
-  if (block < in_full) {
-    const int grp = int(block / ((long long)kGroupHeads * ntiles));
-    const int idx = int(block - (long long)grp * kGroupHeads * ntiles);
-    t.rank = idx / kGroupHeads;
-    t.bh = grp * kGroupHeads + idx % kGroupHeads;
-  } else {
-    const int rest = BH - full;
-    const int idx = int(block - in_full);
-    t.rank = idx / rest;
-    t.bh = full + idx % rest;
-  }
-  return t;
 }
 
 // ---------------------------------------------------------------- preparation
@@ -275,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kBarOff + 196);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const TileOrder to = tile_order(int(blockIdx.x), p.BH, (p.Lk + 127) / 128);
+  const TileOrder to = grouped_tile_order(blockIdx.x, p.BH, (p.Lk + 127) / 128, p.group);
   const int jt = to.rank;      // key tile (the most query tiles first when causal)
   const int bh = to.bh;
   const int nq_all = (p.Lq + 127) / 128;
@@ -486,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nq_all = (p.Lq + 127) / 128;
-  const TileOrder to = tile_order(int(blockIdx.x), p.BH, nq_all);
+  const TileOrder to = grouped_tile_order(blockIdx.x, p.BH, nq_all, p.group);
   const int itile = nq_all - 1 - to.rank;  // the most key tiles first when causal
   const int bh = to.bh;
   const int nk_all = (p.Lk + 127) / 128;
@@ -687,10 +661,12 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
   if (nk > 0x7fffffffLL || nq > 0x7fffffffLL) return -2;
   p.out_a = static_cast<__nv_bfloat16*>(dk);
   p.out_b = static_cast<__nv_bfloat16*>(dv);
+  p.group = l2_head_group(BH, 2ll * Lq * D * 2);   // Q and dO of a head
   fa_bwd_dkdv_kernel<D><<<dim3(unsigned(nk)), dim3(kThreads), CK::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return -4;
   p.out_a = static_cast<__nv_bfloat16*>(dq);
   p.out_b = nullptr;
+  p.group = l2_head_group(BH, 2ll * Lk * D * 2);   // K and V of a head
   fa_bwd_dq_kernel<D><<<dim3(unsigned(nq)), dim3(kThreads), CQ::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

@@ -55,6 +55,48 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
 
 int num_sms_of_current_device(int* num_sms);
 
+// Grid order for work in tiles of whole heads: heads in groups of `group`, all
+// tiles of a group before the next group, so that the CTAs resident at one
+// time share a few heads' K/V (or Q/dO) in L2 instead of streaming every
+// head's from HBM; within a group, rank 0 of every head first, then rank 1,
+// ... (rank 0 = the most work when causal).  A bijection of [0, BH * ntiles)
+// onto (rank, bh).
+struct TileOrder {
+  int rank, bh;
+};
+__host__ __device__ inline TileOrder grouped_tile_order(long long block, int BH, int ntiles, int group) {
+  const int full = BH / group * group;   // heads in whole groups
+  const long long in_full = (long long)full * ntiles;
+  TileOrder t;
+  if (block < in_full) {
+    const long long per = (long long)group * ntiles;
+    const int grp = int(block / per);
+    const int idx = int(block - grp * per);
+    t.rank = idx / group;
+    t.bh = grp * group + idx % group;
+  } else {
+    const int rest = BH - full;
+    const int idx = int(block - in_full);
+    t.rank = idx / rest;
+    t.bh = full + idx % rest;
+  }
+  return t;
+}
+// Heads per group: as many as keep `bytes_per_head` of streamed tiles within
+// FA_L2_GROUP_BUDGET_MB (default 24 MB; 24 to 48 MB measured best for
+// causal 64K and the D = 64 sweep lengths, against one group of all heads),
+// at least one.
+#ifndef FA_L2_GROUP_BUDGET_MB
+#define FA_L2_GROUP_BUDGET_MB 24
+#endif
+inline int l2_head_group(int BH, long long bytes_per_head) {
+  const long long budget = (long long)FA_L2_GROUP_BUDGET_MB << 20;
+  long long g = bytes_per_head > 0 ? budget / bytes_per_head : BH;
+  if (g < 1) g = 1;
+  if (g > BH) g = BH;
+  return int(g);
+}
+
 // Workspace memory, stream-ordered on `stream`, from the library's pool of the
 // current device (kept between calls).  Return FA_OK or FA_ERR_CUDA.
 int workspace_alloc(void** ptr, size_t bytes, cudaStream_t stream);

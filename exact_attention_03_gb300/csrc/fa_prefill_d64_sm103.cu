@@ -72,6 +72,7 @@ struct Params {
   int* err;
   int BH, Lq, Lk;
   int n_qblk;  // ceil(Lq / 256)
+  int group;   // heads per group of the grid order (K/V of a group stay in L2)
   int causal;
   float scale_log2;
 };
@@ -128,9 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- which query tiles this CTA owns (heaviest query blocks first)
-  const int qblk = p.n_qblk - 1 - int(blockIdx.x) / p.BH;
-  const int bh = int(blockIdx.x) % p.BH;
+  // ---- which query tiles this CTA owns (heads in groups whose K/V stay in
+  // L2; within a group the heaviest query blocks first)
+  const TileOrder to = grouped_tile_order(blockIdx.x, p.BH, p.n_qblk, p.group);
+  const int qblk = p.n_qblk - 1 - to.rank;
+  const int bh = to.bh;
   const int q0 = qblk * 256;
   const int nk_all = (p.Lk + 127) / 128;
   // key tiles of query tile 0 and 1; nt0 >= 1, and nt1 is 0 (tile 1 past the
@@ -448,6 +451,7 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
   p.Lq = Lq;
   p.Lk = Lk;
   p.n_qblk = (Lq + 255) / 256;
+  p.group = l2_head_group(BH, 2ll * Lk * 64 * 2);   // K and V of a head
   p.causal = causal;
   p.scale_log2 = scale * 1.44269504088896340736f;
   if (cudaFuncSetAttribute(fa_prefill_d64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
