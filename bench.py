@@ -303,6 +303,7 @@ def per_config(args, fa, flush, dev, peaks, check):
     out.update(per_config_paged(fa, flush, dev, peaks, check))
     out.update(per_config_softmax(fa, flush, dev, peaks, check))
     out.update(per_config_backward(fa, flush, dev, peaks, check))
+    out.update(per_config_dropout(fa, flush, dev, peaks, check))
     return out
 
 
@@ -333,6 +334,35 @@ def per_config_backward(fa, flush, dev, peaks, check):
                                        "launches": 3, "flops_counted": flops}
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
+    return out
+
+
+def per_config_dropout(fa, flush, dev, peaks, check):
+    """The forward with dropout on the weights (fa_fwd_dropout, p = 0.1) on
+    the causal 8K D128 workload and the D64 sweep's 8K length, next to the
+    plain forward on the same inputs: TFLOPS count the same products (the
+    Philox bits are extra work, not extra flops)."""
+    import torch
+    from exact_attention_03_gb300.inputs import WORKLOADS, Workload, make_inputs
+    out = {}
+    for name, w in (("dropout_causal_l8k_d128", WORKLOADS["causal_l8k_d128"]),
+                    ("dropout_l8k_d64", Workload("sweep_8192", 4, 8, 8192, 8192, 64, False, seed=1))):
+        q, k, v = make_inputs(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        call = lambda: fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal, out=o, lse=lse)
+        plain = lambda: fa.forward(q, k, v, causal=w.causal, out=o, lse=lse)
+        _time_launches([call, plain], flush, 2)
+        ts = _time_launches([call, plain], flush, 10)
+        check()
+        ms = statistics.median(ts[0::2])
+        ms_plain = statistics.median(ts[1::2])
+        tf = w.flops / (ms * 1e-3) / 1e12
+        out[name] = {"B": w.B, "H": w.H, "L": w.Lq, "D": w.D, "causal": w.causal, "p_drop": 0.1,
+                     "ms": round(ms, 5), "TFLOPS": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+                     "ms_without_dropout": round(ms_plain, 5), "launches": 1}
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
     return out
 
 

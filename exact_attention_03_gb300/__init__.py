@@ -20,7 +20,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGN
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
            "forward", "forward_host", "decode_noalloc", "decode_paged", "softmax_rows",
-           "backward", "EXPORTED_SYMBOLS"]
+           "backward", "forward_dropout", "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -58,6 +58,9 @@ _SIGS = {
                                        ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "fa_fwd_dropout": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                       + [ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
+                          ctypes.c_uint, ctypes.c_void_p]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -156,6 +159,40 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, out=No
                 int(causal), _stream_handle(stream))
     if st != FA_OK:
         raise FlashAttentionError(st)
+    return out, lse
+
+
+def forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0, causal: bool = False,
+                    scale: Optional[float] = None, out=None, lse=None, stream=None):
+    """forward() with dropout on the attention weights, fused into the kernel
+    (fa_fwd_dropout): weights are kept iff their Philox byte >= round(256 p),
+    kept ones scaled by 256 / (256 - round(256 p)); lse is the undropped
+    log-sum-exp.  `seed` (64-bit) and `offset` (32-bit) select the bits."""
+    import torch
+
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, L, D]")
+    B, H, Lq, D = q.shape
+    if k.shape != (B, H, k.shape[2], D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA bf16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    st = load().fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               B, H, Lq, Lk, D, scale, int(causal), float(p_drop),
+                               int(seed) & ((1 << 64) - 1), int(offset) & 0xFFFFFFFF,
+                               _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_fwd_dropout")
     return out, lse
 
 

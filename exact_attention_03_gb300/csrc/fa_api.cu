@@ -202,6 +202,40 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa::launch_prefill(q, k, v, o, lse, B, H, Lq, Lk, D, scale, causal, s, err);
 }
 
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Lq, int Lk, int D, float scale, int causal, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* stream) {
+  // ---- host-side checks, before any CUDA call
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(p_drop) || !(p_drop >= 0.f) || !(p_drop < 1.f)) return FA_ERR_INVALID_ARG;
+  const double tt = std::floor(double(p_drop) * 256.0 + 0.5);
+  if (tt > 255.0) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (causal && Lq != Lk) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (!fa::aligned(q, 16) || !fa::aligned(k, 16) || !fa::aligned(v, 16) || !fa::aligned(o, 16))
+    return FA_ERR_MISALIGNED;
+  if (lse != nullptr && !fa::aligned(lse, 4)) return FA_ERR_MISALIGNED;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  int* err = fa::error_word_ptr(dev);
+  if (err == nullptr) return FA_ERR_CUDA;
+  fa::Dropout dr;
+  dr.on = 1;
+  dr.seed_lo = uint32_t(seed & 0xffffffffull);
+  dr.seed_hi = uint32_t(seed >> 32);
+  dr.offset = offset;
+  dr.t = uint32_t(tt);
+  dr.keep_scale = float(256.0 / (256.0 - tt));
+  return fa::launch_prefill(q, k, v, o, lse, B, H, Lq, Lk, D, scale, causal, s, err, dr);
+}
+
 int fa_last_device_error(void* stream, int* site) {
   if (site != nullptr) *site = 0;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;

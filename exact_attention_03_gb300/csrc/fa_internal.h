@@ -2,6 +2,7 @@
 // unit and the kernel translation units (not part of the public ABI).
 #pragma once
 
+#include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -23,15 +24,26 @@ enum WaitSite : int {
   kSitePageTable = 11,  // not a wait: a page id outside the paged cache (FA_ERR_INVALID_ARG)
 };
 
+// Dropout on the attention weights (fa_fwd_dropout); `on` = 0 is the plain
+// forward.  Bits from the Philox contract in philox.cuh: a key is kept iff its
+// byte >= t, and O is scaled by keep_scale = 256 / (256 - t).
+struct Dropout {
+  int on = 0;
+  uint32_t seed_lo = 0, seed_hi = 0, offset = 0;
+  uint32_t t = 0;
+  float keep_scale = 1.f;
+};
+
 // Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err);
+                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err,
+                   const Dropout& dr = Dropout());
 
 // Head dimension 64 (Lq >= 1): separate P buffer, one MMA issuer per query tile,
 // the two query tiles' softmax groups half an iteration apart.
 int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
-                       int* err);
+                       int* err, const Dropout& dr = Dropout());
 
 // Single-query split-K/V path (Lq == 1).  Arguments already validated.
 // `workspace` must hold n_split * B * H * (D + 2) floats.

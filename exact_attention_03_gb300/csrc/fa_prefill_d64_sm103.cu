@@ -28,6 +28,7 @@
 // 2 = TMA producer for V, 3 = MMA issue for Q1, 4-7 = softmax of Q0,
 // 8-11 = softmax of Q1.
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
@@ -75,6 +76,10 @@ struct Params {
   int group;   // heads per group of the grid order (K/V of a group stay in L2)
   int causal;
   float scale_log2;
+  // dropout on the weights (the DROP instantiation only): bits from
+  // philox.cuh's contract, key kept iff its byte >= drop_t, O scaled by keep_scale
+  uint32_t seed_lo, seed_hi, offset, drop_t;
+  float keep_scale;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -99,6 +104,7 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
                fmax3(pm[9], pm[10], pm[11]), fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
 }
 
+template <bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_d64_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
@@ -298,13 +304,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 nm2 = make_float2(0.f, 0.f);
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
+        uint4 dw;   // dropout bits of the current 16 keys
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int e = 32 * cb + 2 * i;
+          if constexpr (DROP)
+            if ((i & 7) == 0)
+              dw = philox4x32_10(make_uint4(uint32_t(j * 128 + e) >> 4, uint32_t(qrow), uint32_t(bh), p.offset),
+                                 p.seed_lo, p.seed_hi);
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
           w[i] = pack_bf16x2(pr.x, pr.y);
+          if constexpr (DROP) {
+            const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
+                                : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
+            w[i] &= dropout_pair_mask(wsel, i & 1, p.drop_t);
+          }
         }
       };
       auto rescale_o = [&]() {
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_pv(t), (n - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
     if (ok && n > 0) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = DROP ? p.keep_scale / l_run : 1.f / l_run;
       const bool valid = qrow < p.Lq;
       __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * kD;
 #pragma unroll 1
@@ -436,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
-                       int* err) {
+                       int* err, const Dropout& dr) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   int st = make_tensor_map_bf16(&mq, q, BH, Lq, kD);
@@ -454,12 +470,17 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
   p.group = l2_head_group(BH, 2ll * Lk * 64 * 2);   // K and V of a head
   p.causal = causal;
   p.scale_log2 = scale * 1.44269504088896340736f;
-  if (cudaFuncSetAttribute(fa_prefill_d64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
-    return -4;
+  p.seed_lo = dr.seed_lo;
+  p.seed_hi = dr.seed_hi;
+  p.offset = dr.offset;
+  p.drop_t = dr.t;
+  p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;
-  fa_prefill_d64_kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
+  auto kernel = dr.on ? fa_prefill_d64_kernel<true> : fa_prefill_d64_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    return -4;
+  kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

@@ -36,6 +36,7 @@
 // softmax has read all of S_t into registers.  The next S_t MMA is issued
 // after PV_t, and tcgen05.mma operations from one thread execute in order.
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
@@ -88,6 +89,10 @@ struct Params {
   int group;   // heads per group of the grid order (K/V of a group stay in L2)
   int causal;
   float scale_log2;  // scale * log2(e)
+  // dropout on the weights (the DROP instantiation only): bits from
+  // philox.cuh's contract, key kept iff its byte >= drop_t, O scaled by keep_scale
+  uint32_t seed_lo, seed_hi, offset, drop_t;
+  float keep_scale;
 };
 
 // Bounded wait that ignores the abort flag: used only to drain this CTA's own
@@ -100,7 +105,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -403,12 +408,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t pk[16];
+        uint4 dw;   // dropout bits of the current 16 keys
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          if constexpr (DROP)
+            if ((i & 7) == 0)
+              dw = philox4x32_10(make_uint4(uint32_t(k0 + 32 * cb + 2 * i) >> 4, uint32_t(qrow), uint32_t(bh),
+                                            p.offset),
+                                 p.seed_lo, p.seed_hi);
           const float2 x = __ffma2_rn(make_float2(s[32 * cb + 2 * i], s[32 * cb + 2 * i + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
           pk[i] = pack_bf16x2(pr.x, pr.y);
+          if constexpr (DROP) {
+            const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
+                                : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
+            pk[i] &= dropout_pair_mask(wsel, i & 1, p.drop_t);
+          }
         }
         tmem_st16(tP + 16 * cb, pk);
       }
@@ -439,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), 0, abort_flag, p.err, kSiteSoftmaxO));
     if (ok && n > 0) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = DROP ? p.keep_scale / l_run : 1.f / l_run;
       const bool valid = qrow < p.Lq;
       __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * D;
 #pragma unroll 1
@@ -470,16 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
-           int Lk, float scale, int causal, cudaStream_t stream, int* err);
-
 }  // namespace
 
 namespace {
-template <int D>
+template <int D, bool DROP>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Lq,
-           int Lk, float scale, int causal, cudaStream_t stream, int* err) {
+           int Lk, float scale, int causal, const Dropout& dr, cudaStream_t stream, int* err) {
   using C = Cfg<D>;
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
@@ -499,22 +511,30 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.group = l2_head_group(BH, 2ll * Lk * D * 2);   // K and V of a head
   p.causal = causal;
   p.scale_log2 = scale * 1.44269504088896340736f;
+  p.seed_lo = dr.seed_lo;
+  p.seed_hi = dr.seed_hi;
+  p.offset = dr.offset;
+  p.drop_t = dr.t;
+  p.keep_scale = dr.keep_scale;
 
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");
-  if (cudaFuncSetAttribute(fa_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fa_prefill_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            C::kSmemBytes) != cudaSuccess)
     return -4;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;
-  fa_prefill_kernel<D><<<dim3(unsigned(nblk)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
+  fa_prefill_kernel<D, DROP><<<dim3(unsigned(nblk)), dim3(kThreads), C::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 }  // namespace
 
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err) {
-  if (D == 64) return launch_prefill_d64(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
-  if (D == 128) return launch<128>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
+                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err,
+                   const Dropout& dr) {
+  if (D == 64) return launch_prefill_d64(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err, dr);
+  if (D == 128)
+    return dr.on ? launch<128, true>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, dr, stream, err)
+                 : launch<128, false>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, dr, stream, err);
   return -2;
 }
 

@@ -1,0 +1,59 @@
+// philox.cuh - counter-based random bits for dropout on the attention weights.
+//
+// Philox-4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel Random
+// Numbers: As Easy as 1, 2, 3" (SC 2011), section 3.2: ten rounds over a
+// counter of four 32-bit words under a two-word key; each round multiplies
+// words 0 and 2 by the constants M0 = 0xD2511F53 and M1 = 0xCD9E8D57, keeps
+// both halves of the 64-bit products, and permutes and xors them with the
+// other two words and the round key; the key is bumped by the Weyl constants
+// 0x9E3779B9 and 0xBB67AE85 between rounds.
+//
+// The dropout contract (the library's own: the pages name dropout as the step
+// between softmax and the second matrix product but give no random numbers):
+// key position j of query row i in head bh (= b * H + h) takes byte j mod 4 of
+// word (j div 4) mod 4 of philox(counter = (j div 16, i, bh, offset),
+// key = (seed mod 2^32, seed div 2^32)), and is kept iff that byte >= t.
+#pragma once
+
+#include <cstdint>
+
+namespace fa {
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+
+// Mask for one packed bf16 pair (keys 2m and 2m+1 of a word's four bytes,
+// m = half): 0xffff over each kept element's 16 bits, 0 over a dropped one.
+__device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t word, int half, uint32_t t) {
+  const uint32_t b = word >> (16 * half);
+  const uint32_t m0 = (b & 0xffu) >= t ? 0x0000ffffu : 0u;
+  const uint32_t m1 = ((b >> 8) & 0xffu) >= t ? 0xffff0000u : 0u;
+  return m0 | m1;
+}
+
+// The eight words covering keys k .. k+31 (k a multiple of 32) of one row:
+// two calls, for key groups k/16 and k/16 + 1.
+__device__ __forceinline__ void dropout_words32(uint32_t (&w)[8], uint32_t key0, uint32_t row, uint32_t bh,
+                                                uint32_t offset, uint32_t seed_lo, uint32_t seed_hi) {
+  const uint4 a = philox4x32_10(make_uint4(key0 >> 4, row, bh, offset), seed_lo, seed_hi);
+  const uint4 b = philox4x32_10(make_uint4((key0 >> 4) + 1u, row, bh, offset), seed_lo, seed_hi);
+  w[0] = a.x;
+  w[1] = a.y;
+  w[2] = a.z;
+  w[3] = a.w;
+  w[4] = b.x;
+  w[5] = b.y;
+  w[6] = b.z;
+  w[7] = b.w;
+}
+
+}  // namespace fa

@@ -217,10 +217,31 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
            int D, float scale, int causal, void* stream);
 
+/*
+ * fa_fwd_dropout - fa_fwd with dropout on the attention weights, fused into the
+ * kernel ("6.3 FlashAttention", section "6.3.3 FlashAttention Forward
+ * Process", "Kernel Fusion": scale -> mask -> softmax -> dropout -> matrix
+ * product, all on one tile in on-chip memory).  The pages give no random
+ * number contract; this library's is:
+ *   t = floor(256 * p_drop + 0.5) (in double precision), 0 <= t <= 255;
+ *   key j of query row i in head bh = b * H + h takes byte (j mod 4) of word
+ *   ((j div 4) mod 4) of Philox-4x32-10 (Salmon et al., SC 2011) with
+ *   counter (j div 16, i, bh, offset) and key (seed mod 2^32, seed div 2^32),
+ *   and is kept iff that byte >= t;
+ *   O = ((w * keep) v) * 256 / (256 - t), w = the softmax weights;
+ *   lse = the undropped log-sum-exp (exactly fa_fwd's).
+ * Same arguments and rules as fa_fwd, plus p_drop in [0, 1) with t <= 255
+ * (else FA_ERR_INVALID_ARG), seed and offset.  Every shape, Lq == 1 included,
+ * runs on the prefill kernels.  Errors and asynchrony as for fa_fwd.
+ */
+int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int Lq, int Lk, int D, float scale, int causal, float p_drop,
+                   unsigned long long seed, unsigned int offset, void* stream);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 3)
+#define FA_ABI_VERSION ((1 << 16) | 4)
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,8 @@ def declared_functions():
 def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
-              "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows"):
+              "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows",
+              "fa_bwd", "fa_fwd_dropout"):
         assert n in names
 
 
@@ -41,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16) | 3
+    assert lib.fa_abi_version() == (1 << 16) | 4
 
 
 def test_strerror_covers_every_status(lib):
@@ -212,3 +213,34 @@ def test_bwd_bad_arguments_rejected_on_host(lib, kw, expect):
     a.update(kw)
     assert lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
                       a["B"], a["H"], a["Lq"], a["Lk"], a["D"], a["scale"], a["causal"], None) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(p=-0.1), fa.FA_ERR_INVALID_ARG),
+    (dict(p=1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(p=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(p=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(p=0.999), fa.FA_ERR_INVALID_ARG),      # rounds to 256/256
+    (dict(D=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=1, Lq=64, Lk=128), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_dropout_bad_arguments_rejected_on_host(lib, kw, expect):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Lq=128, Lk=128, D=128, scale=0.1, causal=0, p=0.1,
+             seed=1, offset=0)
+    a.update(kw)
+    assert lib.fa_fwd_dropout(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Lq"], a["Lk"],
+                              a["D"], a["scale"], a["causal"], a["p"], a["seed"], a["offset"], None) == expect
+
+
+def test_dropout_valid_arguments_without_a_gpu_report_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (the fake pointers must never reach a kernel)")
+    assert lib.fa_fwd_dropout(A, A, A, A, A, 1, 1, 128, 128, 64, 0.1, 0, 0.998, (1 << 64) - 1, 7, None) == fa.FA_ERR_CUDA
