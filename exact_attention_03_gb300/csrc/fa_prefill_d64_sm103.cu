@@ -77,8 +77,8 @@ struct Params {
   int causal;
   float scale_log2;
   // dropout on the weights (the DROP instantiation only): bits from
-  // philox.cuh's contract, key kept iff its byte >= drop_t, O scaled by keep_scale
-  uint32_t seed_lo, seed_hi, offset, drop_t;
+  // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
+  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
   float keep_scale;
 };
 
@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 nm2 = make_float2(0.f, 0.f);
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
-        uint4 dw;   // dropout bits of the current 16 keys
+        uint4 dw;          // dropout bits of the current 16 keys
+        uint32_t keep4;    // keep bytes of the current 4 keys
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int e = 32 * cb + 2 * i;
@@ -317,9 +318,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
           w[i] = pack_bf16x2(pr.x, pr.y);
           if constexpr (DROP) {
-            const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
-                                : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
-            w[i] &= dropout_pair_mask(wsel, i & 1, p.drop_t);
+            if ((i & 1) == 0) {
+              const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
+                                  : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
+              keep4 = __vcmpgeu4(wsel, p.drop_t4);
+            }
+            w[i] &= dropout_pair_mask(keep4, i & 1);
           }
         }
       };
@@ -473,7 +477,7 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
   p.seed_lo = dr.seed_lo;
   p.seed_hi = dr.seed_hi;
   p.offset = dr.offset;
-  p.drop_t = dr.t;
+  p.drop_t4 = dr.t * 0x01010101u;
   p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;

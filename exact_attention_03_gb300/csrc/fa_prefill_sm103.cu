@@ -90,8 +90,8 @@ struct Params {
   int causal;
   float scale_log2;  // scale * log2(e)
   // dropout on the weights (the DROP instantiation only): bits from
-  // philox.cuh's contract, key kept iff its byte >= drop_t, O scaled by keep_scale
-  uint32_t seed_lo, seed_hi, offset, drop_t;
+  // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
+  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
   float keep_scale;
 };
 
@@ -408,7 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t pk[16];
-        uint4 dw;   // dropout bits of the current 16 keys
+        uint4 dw;          // dropout bits of the current 16 keys
+        uint32_t keep4;    // keep bytes of the current 4 keys
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if constexpr (DROP)
@@ -421,9 +422,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
           pk[i] = pack_bf16x2(pr.x, pr.y);
           if constexpr (DROP) {
-            const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
-                                : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
-            pk[i] &= dropout_pair_mask(wsel, i & 1, p.drop_t);
+            if ((i & 1) == 0) {
+              const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
+                                  : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
+              keep4 = __vcmpgeu4(wsel, p.drop_t4);
+            }
+            pk[i] &= dropout_pair_mask(keep4, i & 1);
           }
         }
         tmem_st16(tP + 16 * cb, pk);
@@ -514,7 +518,7 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.seed_lo = dr.seed_lo;
   p.seed_hi = dr.seed_hi;
   p.offset = dr.offset;
-  p.drop_t = dr.t;
+  p.drop_t4 = dr.t * 0x01010101u;
   p.keep_scale = dr.keep_scale;
 
   static_assert(C::kSmemBytes <= 232448, "shared memory budget");

@@ -31,29 +31,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
-// Mask for one packed bf16 pair (keys 2m and 2m+1 of a word's four bytes,
-// m = half): 0xffff over each kept element's 16 bits, 0 over a dropped one.
-__device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t word, int half, uint32_t t) {
-  const uint32_t b = word >> (16 * half);
-  const uint32_t m0 = (b & 0xffu) >= t ? 0x0000ffffu : 0u;
-  const uint32_t m1 = ((b >> 8) & 0xffu) >= t ? 0xffff0000u : 0u;
-  return m0 | m1;
-}
-
-// The eight words covering keys k .. k+31 (k a multiple of 32) of one row:
-// two calls, for key groups k/16 and k/16 + 1.
-__device__ __forceinline__ void dropout_words32(uint32_t (&w)[8], uint32_t key0, uint32_t row, uint32_t bh,
-                                                uint32_t offset, uint32_t seed_lo, uint32_t seed_hi) {
-  const uint4 a = philox4x32_10(make_uint4(key0 >> 4, row, bh, offset), seed_lo, seed_hi);
-  const uint4 b = philox4x32_10(make_uint4((key0 >> 4) + 1u, row, bh, offset), seed_lo, seed_hi);
-  w[0] = a.x;
-  w[1] = a.y;
-  w[2] = a.z;
-  w[3] = a.w;
-  w[4] = b.x;
-  w[5] = b.y;
-  w[6] = b.z;
-  w[7] = b.w;
+// Masks for packed bf16 pairs: `keep4` = __vcmpgeu4(word, t * 0x01010101)
+// holds 0xff in each kept key's byte and 0 in each dropped one; the pair of
+// keys 2m, 2m+1 (m = half) of that word gets 0xffff over each kept element's
+// 16 bits and 0 over a dropped one.
+__device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t keep4, int half) {
+  return __byte_perm(keep4, 0u, half ? 0x3322u : 0x1100u);
 }
 
 }  // namespace fa
