@@ -49,12 +49,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-PREFILL_SOURCES = ("exact_attention_03_gb300/csrc/fa_prefill_sm103.cu",
-                   "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
-PREFILL_D64_SOURCES = ("exact_attention_03_gb300/csrc/fa_prefill_d64_sm103.cu",
-                       "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
-DECODE_SOURCES = ("exact_attention_03_gb300/csrc/fa_decode_sm103.cu",
-                  "exact_attention_03_gb300/csrc/sm103_ptx.cuh")
+_CSRC = "exact_attention_03_gb300/csrc/"
+PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_sm103.cu", "sm103_ptx.cuh", "fa_internal.h", "philox.cuh"))
+PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
+                                                "philox.cuh"))
+DECODE_SOURCES = tuple(_CSRC + f for f in ("fa_decode_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
+BACKWARD_SOURCES = tuple(_CSRC + f for f in ("fa_backward_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 
 
 def measured_traffic(key, sources):
@@ -331,7 +331,8 @@ def per_config_backward(fa, flush, dev, peaks, check):
     out["backward_causal_l8k_d128"] = {"B": w.B, "H": w.H, "L": w.Lq, "D": w.D, "causal": True,
                                        "ms": round(ms, 5), "TFLOPS": round(tf, 2),
                                        "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
-                                       "launches": 3, "flops_counted": flops}
+                                       "launches": 3, "flops_counted": flops,
+                                       "traffic": measured_traffic("fa_bwd/causal_l8k_d128", BACKWARD_SOURCES)}
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
     return out
@@ -500,11 +501,22 @@ def run_profile_case(args):
     if args.profile_batch:
         w = w.with_(B=args.profile_batch)
     q, k, v = make_inputs(w, "cuda")
+    if args.profile_op == "forward":
+        call = lambda: fa.forward(q, k, v, causal=w.causal)
+    elif args.profile_op == "dropout":
+        call = lambda: fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal)
+    elif args.profile_op == "backward":
+        g = torch.Generator(device="cuda").manual_seed(11)
+        do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+        o, lse = fa.forward(q, k, v, causal=w.causal)
+        call = lambda: fa.backward(q, k, v, o, lse, do, causal=w.causal)
+    else:
+        raise SystemExit(f"unknown --profile-op {args.profile_op}")
     torch.cuda.synchronize()
     for _ in range(args.reps):
-        fa.forward(q, k, v, causal=w.causal)
+        call()
     st, site = fa.last_device_error()
-    print(json.dumps({"profile_case": w.name, "B": w.B, "reps": args.reps, "status": st}))
+    print(json.dumps({"profile_case": w.name, "op": args.profile_op, "B": w.B, "reps": args.reps, "status": st}))
     if st != fa.FA_OK:
         sys.exit(1)
 
@@ -520,6 +532,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-case", default=None, help="run one workload (for ncu captures)")
     ap.add_argument("--profile-batch", type=int, default=0, help="batch override for --profile-case")
+    ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward"],
+                    help="operation run by --profile-case")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
