@@ -212,9 +212,12 @@ def run_ours(args, rank, world):
         per_len[str(w.Lq)] = {"ms": round(ms, 5), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}
 
     # ---- e2e: the same sweep through the host-buffer API
-    host = [(w, *(t.cpu().pin_memory() for t in (q, k, v))) for (w, q, k, v, _, _) in bufs]
-    for (w, qh, kh, vh) in host:
-        fa.forward_host(qh, kh, vh, causal=w.causal)
+    host = [(w, *(t.cpu().pin_memory() for t in (q, k, v)),
+             torch.empty((w.B, w.H, w.Lq, w.D), dtype=torch.bfloat16, pin_memory=True),
+             torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, pin_memory=True))
+            for (w, q, k, v, _, _) in bufs]
+    for (w, qh, kh, vh, oh, lh) in host:
+        fa.forward_host(qh, kh, vh, causal=w.causal, out=oh, lse=lh)
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(args.steps):
@@ -223,13 +226,13 @@ def run_ours(args, rank, world):
         e1 = torch.cuda.Event(enable_timing=True)
         flush.zero_()
         e0.record(s)
-        for (w, qh, kh, vh) in host:
-            fa.forward_host(qh, kh, vh, causal=w.causal)
+        for (w, qh, kh, vh, oh, lh) in host:
+            fa.forward_host(qh, kh, vh, causal=w.causal, out=oh, lse=lh)
         e1.record(s)
         s.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
     check()
-    h2d = sum(t.numel() * t.element_size() for (_, qh, kh, vh) in host for t in (qh, kh, vh))
+    h2d = sum(t.numel() * t.element_size() for (_, qh, kh, vh, _, _) in host for t in (qh, kh, vh))
     d2h = sum(w.B * w.H * w.Lq * (w.D * 2 + 4) for w in ws)
     e2e_value = job_throughput(step_flops, max_over_ranks(statistics.mean(e2e_ms), world), world)
 

@@ -61,6 +61,9 @@ _SIGS = {
     "fa_fwd_dropout": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                        + [ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
                           ctypes.c_uint, ctypes.c_void_p]),
+    "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                    + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "fa_host_num_chunks": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_longlong]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -320,22 +323,34 @@ def softmax_rows(x, out=None, lse=None, return_lse: bool = True, stream=None):
     return out, lse
 
 
-def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None,
-                 device="cuda", stream=None):
-    """End-to-end call on host tensors: copies q, k, v (pinned CPU bf16) to the
-    device, runs the forward pass and copies O and LSE back into pinned host
-    tensors.  Returns (O, LSE) on the host after synchronising the stream."""
+def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
+                 stream=None):
+    """End-to-end call on host tensors through fa_fwd_host: q, k, v are CPU
+    bf16 [B,H,L,D] tensors (page-locked for full copy bandwidth), O and LSE
+    come back in page-locked CPU tensors.  The library pipelines the copies
+    with the computation over chunks of heads and returns once the outputs
+    are on the host."""
     import torch
 
-    s = torch.cuda.current_stream() if stream is None else stream
-    with torch.cuda.stream(s):
-        qd = q.to(device, non_blocking=True)
-        kd = k.to(device, non_blocking=True)
-        vd = v.to(device, non_blocking=True)
-        o, lse = forward(qd, kd, vd, causal=causal, scale=scale, stream=s)
-        oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
-    s.synchronize()
-    return oh, lh
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, L, D]")
+    B, H, Lq, D = q.shape
+    if k.shape != (B, H, k.shape[2], D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or t.is_cuda:
+            raise ValueError(f"{name} must be a CPU bf16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    Lk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, Lq), dtype=torch.float32, pin_memory=True)
+    st = load().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            B, H, Lq, Lk, D, scale, int(causal), _stream_handle(stream))
+    if st != FA_OK:
+        raise FlashAttentionError(st, "fa_fwd_host")
+    return out, lse

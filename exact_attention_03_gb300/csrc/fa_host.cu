@@ -1,0 +1,170 @@
+// fa_host.cu - attention on host buffers, with the host<->device copies
+// overlapped with the kernels (fa_fwd_host).
+//
+// Heads are independent problems, so one call is split into chunks of
+// consecutive heads (the [B, H, L, D] layout keeps a chunk contiguous) and run
+// as a three-stage pipeline on three streams: the copies of chunk i+1 into the
+// device run while chunk i is computed on the caller's stream and the output of
+// chunk i-1 is copied back.  The two copy directions use separate copy engines,
+// and the device memory holds two chunks (double buffering from the library's
+// workspace pool).  Events order the stages:
+//   copy-in i    after compute i-2 (its input slot is free)
+//   compute i    after copy-in i and after copy-out i-2 (its output slot is free)
+//   copy-out i   after compute i
+// The call returns when the outputs are in host memory.
+#include "fa.h"
+#include "fa_internal.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace fa {
+namespace {
+
+constexpr int kMaxChunks = 8;
+constexpr long long kMinChunkBytes = 8ll << 20;   // below this a chunk's copy is latency-bound
+constexpr int kMaxDevices = 64;
+
+// per-device copy streams and events, created once; calls on one device are
+// serialised by a mutex because they share them
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t in_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {}, out_done[kMaxChunks] = {};
+};
+
+HostPipe* host_pipe(int dev) {
+  static HostPipe pipes[kMaxDevices];
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  return &pipes[dev];
+}
+
+bool init_pipe(HostPipe& p) {
+  if (p.ready) return true;
+  if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess) return false;
+  for (int i = 0; i < kMaxChunks; ++i)
+    if (cudaEventCreateWithFlags(&p.in_done[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.out_done[i], cudaEventDisableTiming) != cudaSuccess)
+      return false;
+  p.ready = true;
+  return true;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_host_num_chunks(long long BH, long long bytes_per_head) {
+  if (BH <= 0 || bytes_per_head <= 0) return 1;
+  long long n = BH * bytes_per_head / fa::kMinChunkBytes;   // at least 8 MiB per chunk
+  n = std::max(1ll, std::min<long long>(n, fa::kMaxChunks));
+  n = std::min(n, BH);
+  const long long hc = (BH + n - 1) / n;                      // heads per chunk
+  return int((BH + hc - 1) / hc);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Lq, int Lk, int D, float scale, int causal, void* stream) {
+  // ---- host-side checks (as fa_fwd), before any CUDA call
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+  if (causal && Lq != Lk) return FA_ERR_UNSUPPORTED;
+  const long long BH = (long long)B * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+
+  const size_t qb = size_t(Lq) * D * 2, kb = size_t(Lk) * D * 2, lb = size_t(Lq) * 4;
+  const int n = fa_host_num_chunks(BH, (long long)(2 * qb + 2 * kb + lb));
+  const long long hc = (BH + n - 1) / n;
+  // one slot: q, k, v, o, lse of hc heads, each part 256-byte aligned
+  const size_t oq = 0, ok_ = fa::round_up(oq + hc * qb, 256), ov = fa::round_up(ok_ + hc * kb, 256),
+               oo = fa::round_up(ov + hc * kb, 256), ol = fa::round_up(oo + hc * qb, 256),
+               slot_bytes = fa::round_up(ol + hc * lb, 256);
+  const int slots = std::min(n, 2);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  fa::HostPipe* pipe = fa::host_pipe(dev);
+  if (pipe == nullptr) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(pipe->mu);
+  if (!fa::init_pipe(*pipe)) return FA_ERR_CUDA;
+
+  void* ws = nullptr;
+  if (fa::workspace_alloc(&ws, slots * slot_bytes, s) != FA_OK) return FA_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  const uint8_t* hq = static_cast<const uint8_t*>(q);
+  const uint8_t* hk = static_cast<const uint8_t*>(k);
+  const uint8_t* hv = static_cast<const uint8_t*>(v);
+  uint8_t* ho = static_cast<uint8_t*>(o);
+  uint8_t* hl = reinterpret_cast<uint8_t*>(lse);
+
+  int st = FA_OK;
+  auto ok = [&](cudaError_t e) {
+    if (e != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
+    return st == FA_OK;
+  };
+  // the workspace is ordered on s: the copy streams start after it
+  if (ok(cudaEventRecord(pipe->start, s))) {
+    ok(cudaStreamWaitEvent(pipe->h2d, pipe->start, 0));
+    ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0));
+  }
+  for (int i = 0; i < n && st == FA_OK; ++i) {
+    const long long h0 = i * hc, nh = std::min(hc, BH - h0);
+    uint8_t* slot = base + size_t(i % 2) * slot_bytes;
+    // copy-in of chunk i, once compute i-2 has released the slot's inputs
+    if (i >= 2 && !ok(cudaStreamWaitEvent(pipe->h2d, pipe->comp_done[i - 2], 0))) break;
+    if (!ok(cudaMemcpyAsync(slot + oq, hq + h0 * qb, nh * qb, cudaMemcpyHostToDevice, pipe->h2d)) ||
+        !ok(cudaMemcpyAsync(slot + ok_, hk + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
+        !ok(cudaMemcpyAsync(slot + ov, hv + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
+        !ok(cudaEventRecord(pipe->in_done[i], pipe->h2d)))
+      break;
+    // compute chunk i on the caller's stream (heads h0 .. h0+nh-1 as one batch)
+    if (!ok(cudaStreamWaitEvent(s, pipe->in_done[i], 0))) break;
+    if (i >= 2 && !ok(cudaStreamWaitEvent(s, pipe->out_done[i - 2], 0))) break;
+    const int r = fa_fwd(slot + oq, slot + ok_, slot + ov, slot + oo,
+                         lse != nullptr ? reinterpret_cast<float*>(slot + ol) : nullptr, 1, int(nh), Lq, Lk,
+                         D, scale, causal, s);
+    if (r != FA_OK) {
+      st = r;
+      break;
+    }
+    if (!ok(cudaEventRecord(pipe->comp_done[i], s))) break;
+    // copy-out of chunk i
+    if (!ok(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[i], 0))) break;
+    if (!ok(cudaMemcpyAsync(ho + h0 * qb, slot + oo, nh * qb, cudaMemcpyDeviceToHost, pipe->d2h))) break;
+    if (lse != nullptr && !ok(cudaMemcpyAsync(hl + h0 * lb, slot + ol, nh * lb, cudaMemcpyDeviceToHost, pipe->d2h)))
+      break;
+    if (!ok(cudaEventRecord(pipe->out_done[i], pipe->d2h))) break;
+  }
+  // every copy has finished before the workspace goes back to the pool: on
+  // success the caller's stream waits for the last copy-out; on an error all
+  // three streams are drained first
+  if (st == FA_OK) {
+    // copy-outs run in order on one stream, and every copy-in finished before
+    // the last compute started
+    ok(cudaStreamWaitEvent(s, pipe->out_done[n - 1], 0));
+  } else {
+    cudaStreamSynchronize(pipe->h2d);
+    cudaStreamSynchronize(pipe->d2h);
+    cudaStreamSynchronize(s);
+  }
+  const bool freed = fa::workspace_free(ws, s) == FA_OK;
+  const bool synced = cudaStreamSynchronize(s) == cudaSuccess;
+  if (st != FA_OK) return st;
+  return freed && synced ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -238,10 +238,32 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
                    int H, int Lq, int Lk, int D, float scale, int causal, float p_drop,
                    unsigned long long seed, unsigned int offset, void* stream);
 
+/*
+ * fa_fwd_host - fa_fwd on HOST buffers: q, k, v are read from and o, lse
+ * written to host memory (page-locked memory gives the full copy bandwidth;
+ * pageable memory works, slower).  The heads are split into up to 8 chunks of
+ * consecutive heads (at least 8 MiB of copies each, fa_host_num_chunks), and
+ * the copies of one chunk overlap the computation of the next: copy-in,
+ * compute and copy-out run on three streams (two internal copy streams and
+ * `stream`, which carries the computation), ordered by events, with two
+ * chunks of device memory from the library's pool.  Same argument rules as
+ * fa_fwd (lse may be NULL; host pointers have no alignment rule).  The call
+ * returns after the outputs are in host memory.  Calls on one device are
+ * serialised (they share the copy streams).
+ */
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Lq, int Lk, int D, float scale, int causal, void* stream);
+
+/* fa_host_num_chunks - the number of head chunks fa_fwd_host uses for BH heads
+ * of bytes_per_head copied bytes each: min(8, BH, BH * bytes_per_head / 8 MiB),
+ * at least 1, then rounded so that every chunk but the last has the same
+ * number of heads. */
+int fa_host_num_chunks(long long BH, long long bytes_per_head);
+
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 4)
+#define FA_ABI_VERSION ((1 << 16) | 5)
 
 #ifdef __cplusplus
 }

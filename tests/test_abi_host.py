@@ -30,7 +30,7 @@ def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
               "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows",
-              "fa_bwd", "fa_fwd_dropout"):
+              "fa_bwd", "fa_fwd_dropout", "fa_fwd_host", "fa_host_num_chunks"):
         assert n in names
 
 
@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16) | 4
+    assert lib.fa_abi_version() == (1 << 16) | 5
 
 
 def test_strerror_covers_every_status(lib):
@@ -244,3 +244,31 @@ def test_dropout_valid_arguments_without_a_gpu_report_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("needs a machine without a GPU (the fake pointers must never reach a kernel)")
     assert lib.fa_fwd_dropout(A, A, A, A, A, 1, 1, 128, 128, 64, 0.1, 0, 0.998, (1 << 64) - 1, 7, None) == fa.FA_ERR_CUDA
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(H=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=5), fa.FA_ERR_INVALID_ARG),
+    (dict(D=80), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=1, Lq=64, Lk=128), fa.FA_ERR_UNSUPPORTED),
+])
+def test_host_entry_bad_arguments_rejected_on_host(lib, kw, expect):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=1, H=1, Lq=128, Lk=128, D=128, scale=0.1, causal=0)
+    a.update(kw)
+    assert lib.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Lq"], a["Lk"], a["D"],
+                           a["scale"], a["causal"], None) == expect
+
+
+@pytest.mark.parametrize("BH,per,expect", [(1, 1, 1), (2, 300 * 128 * 8, 1), (32, 8192 * 64 * 8, 8),
+                                           (13, 2048 * 128 * 8, 3), (3, 1 << 30, 3), (1000, 1 << 20, 8),
+                                           (17, 1 << 22, 6), (0, 5, 1), (5, 0, 1)])
+def test_host_chunk_rule(lib, BH, per, expect):
+    # min(8, BH, BH * per / 8 MiB) chunks, at least 1, then as many as equal head counts need
+    n = lib.fa_host_num_chunks(BH, per)
+    assert n == expect
+    if BH > 0 and per > 0:
+        hc = -(-BH // n)
+        assert (n - 1) * hc < BH <= n * hc
