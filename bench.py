@@ -492,34 +492,50 @@ def run_reference(args, rank, world):
 
 def run_profile_case(args):
     """Runs one workload `reps` times with no flush or timing: the command
-    the ncu captures profile."""
+    the ncu captures profile.  `--profile-op` picks the operation: the
+    forward, the forward with dropout or the backward on a prefill workload,
+    the paged decode on a paged workload, or the row softmax (an 8192 x 8192
+    fp32 matrix; the case name is ignored)."""
+    import dataclasses
     import torch
     import exact_attention_03_gb300 as fa
     from exact_attention_03_gb300 import build as fa_build
-    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+    from exact_attention_03_gb300.inputs import PAGED_WORKLOADS, WORKLOADS, make_inputs, make_paged_inputs
 
     fa_build.build()
     fa.load()
-    w = WORKLOADS[args.profile_case]
-    if args.profile_batch:
-        w = w.with_(B=args.profile_batch)
-    q, k, v = make_inputs(w, "cuda")
-    if args.profile_op == "forward":
-        call = lambda: fa.forward(q, k, v, causal=w.causal)
-    elif args.profile_op == "dropout":
-        call = lambda: fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal)
-    elif args.profile_op == "backward":
-        g = torch.Generator(device="cuda").manual_seed(11)
-        do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
-        o, lse = fa.forward(q, k, v, causal=w.causal)
-        call = lambda: fa.backward(q, k, v, o, lse, do, causal=w.causal)
+    name, B = args.profile_case, 0
+    if args.profile_op == "softmax":
+        g = torch.Generator(device="cuda").manual_seed(10)
+        x = torch.randn(8192, 8192, generator=g, device="cuda") * 4
+        call = lambda: fa.softmax_rows(x)
+    elif args.profile_op == "paged":
+        w = PAGED_WORKLOADS[args.profile_case]
+        if args.profile_batch:
+            w = dataclasses.replace(w, B=args.profile_batch)
+        qp, kc, vc, bt, lens = make_paged_inputs(w, "cuda")
+        call = lambda: fa.decode_paged(qp, kc, vc, bt, lens)
+        B = w.B
     else:
-        raise SystemExit(f"unknown --profile-op {args.profile_op}")
+        w = WORKLOADS[args.profile_case]
+        if args.profile_batch:
+            w = w.with_(B=args.profile_batch)
+        B = w.B
+        q, k, v = make_inputs(w, "cuda")
+        if args.profile_op == "forward":
+            call = lambda: fa.forward(q, k, v, causal=w.causal)
+        elif args.profile_op == "dropout":
+            call = lambda: fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal)
+        else:
+            g = torch.Generator(device="cuda").manual_seed(11)
+            do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+            o, lse = fa.forward(q, k, v, causal=w.causal)
+            call = lambda: fa.backward(q, k, v, o, lse, do, causal=w.causal)
     torch.cuda.synchronize()
     for _ in range(args.reps):
         call()
     st, site = fa.last_device_error()
-    print(json.dumps({"profile_case": w.name, "op": args.profile_op, "B": w.B, "reps": args.reps, "status": st}))
+    print(json.dumps({"profile_case": name, "op": args.profile_op, "B": B, "reps": args.reps, "status": st}))
     if st != fa.FA_OK:
         sys.exit(1)
 
@@ -535,7 +551,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-case", default=None, help="run one workload (for ncu captures)")
     ap.add_argument("--profile-batch", type=int, default=0, help="batch override for --profile-case")
-    ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward"],
+    ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward", "paged", "softmax"],
                     help="operation run by --profile-case")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
