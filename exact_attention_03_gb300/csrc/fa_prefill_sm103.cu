@@ -5,7 +5,7 @@
 // streams that head's K/V in 128-key tiles through a shared-memory ring.
 // Both matrix products run on the 5th-generation tensor cores:
 //   S_t = Q_t K_j^T   tcgen05.mma, A = Q_t (smem), B = K_j (smem), fp32 in TMEM
-//   O_t += P_t V_j    tcgen05.mma, A = P_t (TMEM, bf16), B = V_j (smem), fp32 in TMEM
+//   O_t += P_t V_j    tcgen05.mma, A = P_t (smem, bf16), B = V_j (smem), fp32 in TMEM
 // and the softmax runs in between on CUDA cores, one thread per query row.
 //
 // The per-row update is the online-softmax recurrence of "NTU Hung-yi Lee ML
@@ -23,18 +23,23 @@
 //
 // Warp roles (12 warps, 384 threads, one CTA per SM):
 //   warp 0        TMA producer: Q0, Q1 once; then K_0, K_1, ... into the K ring
-//   warp 1        TMEM allocation; lane 0 issues every tcgen05.mma and commit
+//   warp 1        TMEM allocation; lane 0 issues the MMAs of query tile 0
 //   warp 2        TMA producer: V_0, V_1, ... into the V ring
-//   warp 3        idle (keeps the softmax warpgroups aligned to TMEM lane quarters)
+//   warp 3        lane 0 issues the MMAs of query tile 1
 //   warps 4-7     softmax + epilogue for Q0 (TMEM lanes 0-127 = its 128 rows)
 //   warps 8-11    softmax + epilogue for Q1
-// Issue order of the MMA thread (ping-pong between the two query tiles, so the
-// tensor core works on one tile while the other tile's softmax runs):
-//   S0(0) S1(0) | PV0(0) S0(1) PV1(0) S1(1) | PV0(1) S0(2) PV1(1) S1(2) | ...
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D);
-// P_t (bf16 pairs, 64 columns) overwrites columns [64,128) of S_t after the
-// softmax has read all of S_t into registers.  The next S_t MMA is issued
-// after PV_t, and tcgen05.mma operations from one thread execute in order.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// P_t goes to shared memory (128 x 128 bf16 in the 128-byte-swizzled K-major
+// layout of a TMA tile), so S_t(j+1) no longer waits for P_t(j) V: each
+// issuer computes S_t(j) as soon as its softmax group holds S_t(j-1) in
+// registers, and P_t(j-1) V_(j-1) once P_t(j-1) is in shared memory; the
+// softmax computes all 128 weights of a row in registers, then waits for the
+// previous P V (O stable, P buffer free), rescales O if needed and stores P.
+// With P read from shared memory both products stream two operands from it,
+// and its bandwidth bounds the iteration (measured: the P stores wait behind
+// the tensor core's operand reads); against P in TMEM overwriting S, where the
+// next S waited for the P V of the same tile, this runs 3-5 % faster.
+// Shared memory: Q0, Q1, the K ring (2 stages), V (1 stage), P0, P1: 224 KB.
 #include "fa_internal.h"
 #include "philox.cuh"
 #include "sm103_ptx.cuh"
@@ -55,14 +60,15 @@ constexpr int kSubBytes = 128 * 128;  // one 128-row x 64-column bf16 sub-block 
 
 template <int D>
 struct Cfg {
-  static constexpr int kSub = D / 64;              // 128-byte column blocks per row
   static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile (one TMA box)
   static constexpr int kKStages = (D == 128) ? 2 : 4;   // K ring
-  static constexpr int kVStages = (D == 128) ? 2 : 4;   // V ring
+  static constexpr int kVStages = (D == 128) ? 1 : 4;   // V ring
   static constexpr int kQOff = 0;
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kVStages * kTileBytes;
+  static constexpr int kPOff = kVOff + kVStages * kTileBytes;   // P_t: 128 x 128 bf16, K-major SW128
+  static constexpr int kPBytes = 128 * 128 * 2;
+  static constexpr int kBarOff = kPOff + 2 * kPBytes;
   // barriers: q_full[2] kfull[SK] kempty[SK] vfull[SV] vempty[SV] s_full[2] p_full[2] o_full[2] mma_done
   static constexpr int kBarQ = 0;
   static constexpr int kBarKFull = 16;
@@ -72,8 +78,10 @@ struct Cfg {
   static constexpr int kBarS = kBarVEmpty + 8 * kVStages;
   static constexpr int kBarP = kBarS + 16;
   static constexpr int kBarO = kBarP + 16;
-  static constexpr int kBarDone = kBarO + 16;
-  static constexpr int kTmemHolder = kBarDone + 8;
+  static constexpr int kBarSFree = kBarO + 16;
+  static constexpr int kBarPV = kBarSFree + 16;
+  static constexpr int kBarDone = kBarPV + 16;
+  static constexpr int kTmemHolder = kBarDone + 16;   // after the two issuers' done barriers
   static constexpr int kAbort = kTmemHolder + 4;
   static constexpr int kMiscBytes = 256;
   static_assert(kAbort + 4 <= kMiscBytes, "barrier area overflow");
@@ -130,7 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_s = [&](int t) { return sBar + C::kBarS + 8 * t; };
   auto bar_p = [&](int t) { return sBar + C::kBarP + 8 * t; };
   auto bar_o = [&](int t) { return sBar + C::kBarO + 8 * t; };
+  auto bar_sfree = [&](int t) { return sBar + C::kBarSFree + 8 * t; };
+  auto bar_pv = [&](int t) { return sBar + C::kBarPV + 8 * t; };
   const uint32_t bar_done = sBar + C::kBarDone;
+  const uint32_t sP = base + C::kPOff;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,20 +172,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q(0), 1);
     mbar_init(bar_q(1), 1);
+    // each MMA issuer releases every ring stage once (count 2 when both query
+    // tiles have work)
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(bar_kfull(s), 1);
-      mbar_init(bar_kempty(s), 1);
+      mbar_init(bar_kempty(s), nt[1] > 0 ? 2 : 1);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(bar_vfull(s), 1);
-      mbar_init(bar_vempty(s), 1);
+      mbar_init(bar_vempty(s), nt[1] > 0 ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s(t), 1);
       mbar_init(bar_p(t), 128);
       mbar_init(bar_o(t), 1);
+      mbar_init(bar_sfree(t), 128);
+      mbar_init(bar_pv(t), 1);
     }
     mbar_init(bar_done, 1);
+    mbar_init(bar_done + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -236,13 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(is_k ? bar_kfull(s) : bar_vfull(s), (last / NS) & 1);
       }
     }
-  } else if (warp == 1) {
-    // =================== MMA issuer ===================
+  } else if (warp == 1 || (warp == 3 && nt[1] > 0)) {
+    // =================== MMA issuers: warp 1 for query tile 0, warp 3 for tile 1 ===================
     if (lane == 0) {
+      const int t = (warp == 1) ? 0 : 1;
+      const int n = nt[t];
       constexpr uint32_t kIdQK = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t kIdPV = idesc_bf16_f32(128, D, false, true);
-      // K-major operands (Q, K): 8-row atoms 1024 B apart.  MN-major operand (V):
-      // 8-key groups 1024 B apart, 64-column blocks kSubBytes apart.
       constexpr uint64_t kDescK = sdesc_sw128(0, 16, 1024);
       constexpr uint64_t kDescMN = sdesc_sw128(0, kSubBytes, 1024);
       bool ok = true;
@@ -250,97 +266,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && !mbar_wait(b, ph, abort_flag, p.err, site)) ok = false;
         return ok;
       };
-      // S_t = Q_t K^T: M = 128 rows, N = 128 keys, K = D in steps of 16
-      auto issue_qk = [&](int t, uint32_t kaddr) {
-        const uint32_t a0 = sQ + t * C::kTileBytes;
+      const uint32_t a0 = sQ + t * C::kTileBytes;
+      const uint32_t pt = sP + t * C::kPBytes;
+      wait(bar_q(t), 0, kSiteMmaQ);
+      // j: S_t(j) once K_j is in and the softmax holds S_t(j-1) in registers;
+      // then P_t(j-1) V_(j-1) once P_t(j-1) is in shared memory.  Every key
+      // tile's K and V stages are released by this issuer too.
+      for (int j = 0; j <= nkv && ok; ++j) {
+        if (j < nkv) {
+          const int ks = j % C::kKStages;
+          if (!wait(bar_kfull(ks), (j / C::kKStages) & 1, kSiteMmaK)) break;
+          if (j < n) {
+            if (j > 0 && !wait(bar_sfree(t), (j - 1) & 1, kSiteMmaS)) break;
+            tc_fence_after();
+            const uint32_t kaddr = sK + ks * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
-          umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + off), sdesc_at(kDescK, kaddr + off), kIdQK,
-                  kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+              umma_ss(tmem + t * 128, sdesc_at(kDescK, a0 + off), sdesc_at(kDescK, kaddr + off), kIdQK,
+                      kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar_s(t));
+          }
+          umma_commit(bar_kempty(ks));
         }
-      };
-      // O_t += P_t V: M = 128 rows, N = D, K = 128 keys in steps of 16
-      auto issue_pv = [&](int t, uint32_t vaddr, bool accumulate) {
-        const uint32_t tP = tmem + t * 128 + 64;
-        const uint32_t tO = tmem + 256 + t * D;
+        if (j > 0) {
+          const int vs = (j - 1) % C::kVStages;
+          if (!wait(bar_vfull(vs), ((j - 1) / C::kVStages) & 1, kSiteMmaV)) break;
+          if (j - 1 < n) {
+            if (!wait(bar_p(t), (j - 1) & 1, kSiteMmaP)) break;
+            tc_fence_after();
+            const uint32_t vaddr = sV + vs * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          umma_ts(tO, tP + kk * 8, sdesc_at(kDescMN, vaddr + kk * 16 * 128), kIdPV,
-                  (accumulate || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kSubBytes + (kk & 3) * 32;
+              umma_ss(tmem + 256 + t * D, sdesc_at(kDescK, pt + off),
+                      sdesc_at(kDescMN, vaddr + kk * 16 * 128), kIdPV, (j - 1 > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(bar_pv(t));
+            if (j - 1 == n - 1) umma_commit(bar_o(t));
+          }
+          umma_commit(bar_vempty(vs));
         }
-      };
-
-      // A wait stalls this thread for several hundred cycles, and the tensor
-      // core idles unless that much MMA work is already queued: every wait
-      // below sits between two MMA groups, never two waits in a row.
-      // Ring positions (slot, phase) of K_j and V_j advance incrementally.
-      int ks = 0, vs = 0;
-      uint32_t kph = 0, vph = 0;
-      wait(bar_q(0), 0, kSiteMmaQ);
-      if (nt[1] > 0) wait(bar_q(1), 0, kSiteMmaQ);
-      if (wait(bar_kfull(0), 0, kSiteMmaK)) {
-        tc_fence_after();
-        if (nt[0] > 0) {
-          issue_qk(0, sK);
-          umma_commit(bar_s(0));
-        }
-        if (nt[1] > 0) {
-          issue_qk(1, sK);
-          umma_commit(bar_s(1));
-        }
-        umma_commit(bar_kempty(0));
-      }
-      wait(bar_vfull(0), 0, kSiteMmaV);
-      for (int j = 0; j < nkv && ok; ++j) {
-        const uint32_t vaddr = sV + vs * C::kTileBytes;
-        const int ks1 = (ks + 1 == C::kKStages) ? 0 : ks + 1;
-        const uint32_t kph1 = (ks1 == 0) ? (kph ^ 1u) : kph;
-        const int vs1 = (vs + 1 == C::kVStages) ? 0 : vs + 1;
-        const uint32_t vph1 = (vs1 == 0) ? (vph ^ 1u) : vph;
-        const bool more = (j + 1 < nkv);
-        // PV0(j)
-        if (j < nt[0]) {
-          if (!wait(bar_p(0), j & 1, kSiteMmaP)) break;
-          tc_fence_after();
-          issue_pv(0, vaddr, j > 0);
-          if (j == nt[0] - 1) umma_commit(bar_o(0));
-        }
-        // S0(j+1)
-        if (more) {
-          if (!wait(bar_kfull(ks1), kph1, kSiteMmaK)) break;
-          tc_fence_after();
-        }
-        if (j + 1 < nt[0]) {
-          issue_qk(0, sK + ks1 * C::kTileBytes);
-          umma_commit(bar_s(0));
-        }
-        // PV1(j)
-        if (j < nt[1]) {
-          if (!wait(bar_p(1), j & 1, kSiteMmaP)) break;
-          tc_fence_after();
-          issue_pv(1, vaddr, j > 0);
-          if (j == nt[1] - 1) umma_commit(bar_o(1));
-        }
-        umma_commit(bar_vempty(vs));
-        // S1(j+1); V_{j+1} is waited for here, ahead of the next PV0
-        if (more) {
-          if (!wait(bar_vfull(vs1), vph1, kSiteMmaV)) break;
-          tc_fence_after();
-        }
-        if (j + 1 < nt[1]) {
-          issue_qk(1, sK + ks1 * C::kTileBytes);
-          umma_commit(bar_s(1));
-        }
-        if (more) umma_commit(bar_kempty(ks1));
-        ks = ks1;
-        kph = kph1;
-        vs = vs1;
-        vph = vph1;
       }
       // every MMA issued above has completed before TMEM is released
-      umma_commit(bar_done);
-      drain_wait(bar_done, 0);
+      umma_commit(bar_done + 8 * t);
+      drain_wait(bar_done + 8 * t, 0);
     }
   }
   } else {
@@ -353,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qrow = qt + r;
     const uint32_t lane_off = uint32_t(g * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
-    const uint32_t tP = tS + 64;
+    const uint32_t sPt = sP + t * C::kPBytes;
     const uint32_t tO = tmem + lane_off + 256 + t * D;
     const float c = p.scale_log2;
     float m_run = -INFINITY;  // running max, log2 units
@@ -367,6 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[128];
       tmem_ld128_sync(tS, s);
+      tc_fence_before();
+      mbar_arrive(bar_sfree(t));   // S_t is in registers: the next S_t may be computed
 
       const int k0 = j * 128;
       const bool edge = (k0 + 128 > p.Lk) || (p.causal && k0 + 127 > qt);
@@ -398,16 +371,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float alpha = ex2_approx(m_run - m_safe);    // 0 on the first tile
       m_run = m_use;
 
-      // P = 2^(x - m) in bf16 pairs, written over columns [64,128) of S;
+      // P = 2^(x - m) in bf16 pairs, all 128 keys in registers first;
       // x - m = s * c - m as packed fp32x2 FMAs, row sum in 8 independent chains
       const float2 c2 = make_float2(c, c);
       const float2 nm2 = make_float2(-m_safe, -m_safe);
       float2 acc[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+      uint32_t pk[4][16];
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        uint32_t pk[16];
         uint4 dw;          // dropout bits of the current 16 keys
         uint32_t keep4;    // keep bytes of the current 4 keys
 #pragma unroll
@@ -420,24 +393,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x = __ffma2_rn(make_float2(s[32 * cb + 2 * i], s[32 * cb + 2 * i + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
-          pk[i] = pack_bf16x2(pr.x, pr.y);
+          pk[cb][i] = pack_bf16x2(pr.x, pr.y);
           if constexpr (DROP) {
             if ((i & 1) == 0) {
               const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
                                   : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
               keep4 = __vcmpgeu4(wsel, p.drop_t4);
             }
-            pk[i] &= dropout_pair_mask(keep4, i & 1);
+            pk[cb][i] &= dropout_pair_mask(keep4, i & 1);
           }
         }
-        tmem_st16(tP + 16 * cb, pk);
       }
       const float2 a01 = __fadd2_rn(acc[0], acc[1]);
       const float2 a23 = __fadd2_rn(acc[2], acc[3]);
       const float2 a03 = __fadd2_rn(a01, a23);
       l_run = l_run * alpha + (a03.x + a03.y);
 
-      // rescale O: PV of tile j-1 has completed (S_t(j)'s commit was issued after it)
+      // P_t(j-1) V has completed: O_t is stable and the P_t buffer is free
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv(t), (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (any && j > 0) {
 #pragma unroll 1
         for (int cc = 0; cc < D; cc += 32) {
@@ -449,6 +426,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + cc, w);
         }
       }
+      // P row r into the K-major 128-byte-swizzled tile: keys 8c .. 8c+7 are
+      // 16-byte chunk c, in block c / 8 (16 KB apart), at row r's chunk
+      // position (c mod 8) xor (r mod 8)
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4) {
+          const int ch = 4 * cb + m4;
+          const uint32_t addr = sPt + (ch >> 3) * kSubBytes + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[cb][4 * m4]),
+                       "r"(pk[cb][4 * m4 + 1]), "r"(pk[cb][4 * m4 + 2]), "r"(pk[cb][4 * m4 + 3])
+                       : "memory");
+        }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p(t));
