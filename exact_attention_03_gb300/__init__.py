@@ -64,6 +64,8 @@ _SIGS = {
     "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
                     + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "fa_host_num_chunks": (ctypes.c_int, [ctypes.c_longlong, ctypes.c_longlong]),
+    "fa_fwd_host_async": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                          + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
 }
 EXPORTED_SYMBOLS = tuple(_SIGS)
 
@@ -324,12 +326,14 @@ def softmax_rows(x, out=None, lse=None, return_lse: bool = True, stream=None):
 
 
 def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None, out=None, lse=None,
-                 stream=None):
+                 stream=None, sync: bool = True):
     """End-to-end call on host tensors through fa_fwd_host: q, k, v are CPU
     bf16 [B,H,L,D] tensors (page-locked for full copy bandwidth), O and LSE
     come back in page-locked CPU tensors.  The library pipelines the copies
-    with the computation over chunks of heads and returns once the outputs
-    are on the host."""
+    with the computation over chunks of heads.  With sync (the default) the
+    call returns once the outputs are on the host; with sync=False it returns
+    once the work is queued (fa_fwd_host_async) and the outputs are ready when
+    `stream` (default: the current stream) has been synchronised."""
     import torch
 
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
@@ -349,8 +353,9 @@ def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None, o
         out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, pin_memory=True)
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, pin_memory=True)
-    st = load().fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                            B, H, Lq, Lk, D, scale, int(causal), _stream_handle(stream))
+    fn = load().fa_fwd_host if sync else load().fa_fwd_host_async
+    st = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            B, H, Lq, Lk, D, scale, int(causal), _stream_handle(stream))
     if st != FA_OK:
-        raise FlashAttentionError(st, "fa_fwd_host")
+        raise FlashAttentionError(st, "fa_fwd_host" if sync else "fa_fwd_host_async")
     return out, lse

@@ -6,12 +6,15 @@
 // as a three-stage pipeline on three streams: the copies of chunk i+1 into the
 // device run while chunk i is computed on the caller's stream and the output of
 // chunk i-1 is copied back.  The two copy directions use separate copy engines,
-// and the device memory holds two chunks (double buffering from the library's
-// workspace pool).  Events order the stages:
-//   copy-in i    after compute i-2 (its input slot is free)
-//   compute i    after copy-in i and after copy-out i-2 (its output slot is free)
+// and the device memory holds three chunks (from the library's workspace
+// pool).  Events order the stages:
+//   copy-in i    after compute i-3 (its input slot is free)
+//   compute i    after copy-in i and after copy-out i-3 (its output slot is free)
 //   copy-out i   after compute i
-// The call returns when the outputs are in host memory.
+// fa_fwd_host returns when the outputs are in host memory; fa_fwd_host_async
+// returns once the work is queued (complete when `stream` reaches that point),
+// so that the copy-in of the next call runs while this one computes: the
+// workspace is taken on the copy-in stream, not behind the caller's stream.
 #include "fa.h"
 #include "fa_internal.h"
 
@@ -24,6 +27,7 @@ namespace fa {
 namespace {
 
 constexpr int kMaxChunks = 8;
+constexpr int kSlots = 3;      // chunks of device memory in flight
 constexpr long long kMinChunkBytes = 8ll << 20;   // below this a chunk's copy is latency-bound
 constexpr int kMaxDevices = 64;
 
@@ -73,8 +77,8 @@ int fa_host_num_chunks(long long BH, long long bytes_per_head) {
   return int((BH + hc - 1) / hc);
 }
 
-int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int Lq, int Lk, int D, float scale, int causal, void* stream) {
+int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                      int Lq, int Lk, int D, float scale, int causal, void* stream) {
   // ---- host-side checks (as fa_fwd), before any CUDA call
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
@@ -92,7 +96,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   const size_t oq = 0, ok_ = fa::round_up(oq + hc * qb, 256), ov = fa::round_up(ok_ + hc * kb, 256),
                oo = fa::round_up(ov + hc * kb, 256), ol = fa::round_up(oo + hc * qb, 256),
                slot_bytes = fa::round_up(ol + hc * lb, 256);
-  const int slots = std::min(n, 2);
+  const int slots = std::min(n, fa::kSlots);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -102,8 +106,10 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   std::lock_guard<std::mutex> lock(pipe->mu);
   if (!fa::init_pipe(*pipe)) return FA_ERR_CUDA;
 
+  // the workspace is ordered on the copy-in stream: the other two streams
+  // start after the allocation point
   void* ws = nullptr;
-  if (fa::workspace_alloc(&ws, slots * slot_bytes, s) != FA_OK) return FA_ERR_CUDA;
+  if (fa::workspace_alloc(&ws, slots * slot_bytes, pipe->h2d) != FA_OK) return FA_ERR_CUDA;
   uint8_t* base = static_cast<uint8_t*>(ws);
   const uint8_t* hq = static_cast<const uint8_t*>(q);
   const uint8_t* hk = static_cast<const uint8_t*>(k);
@@ -116,16 +122,15 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     if (e != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
     return st == FA_OK;
   };
-  // the workspace is ordered on s: the copy streams start after it
-  if (ok(cudaEventRecord(pipe->start, s))) {
-    ok(cudaStreamWaitEvent(pipe->h2d, pipe->start, 0));
+  if (ok(cudaEventRecord(pipe->start, pipe->h2d))) {
+    ok(cudaStreamWaitEvent(s, pipe->start, 0));
     ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0));
   }
   for (int i = 0; i < n && st == FA_OK; ++i) {
     const long long h0 = i * hc, nh = std::min(hc, BH - h0);
-    uint8_t* slot = base + size_t(i % 2) * slot_bytes;
-    // copy-in of chunk i, once compute i-2 has released the slot's inputs
-    if (i >= 2 && !ok(cudaStreamWaitEvent(pipe->h2d, pipe->comp_done[i - 2], 0))) break;
+    uint8_t* slot = base + size_t(i % fa::kSlots) * slot_bytes;
+    // copy-in of chunk i, once compute i-3 has released the slot's inputs
+    if (i >= fa::kSlots && !ok(cudaStreamWaitEvent(pipe->h2d, pipe->comp_done[i - fa::kSlots], 0))) break;
     if (!ok(cudaMemcpyAsync(slot + oq, hq + h0 * qb, nh * qb, cudaMemcpyHostToDevice, pipe->h2d)) ||
         !ok(cudaMemcpyAsync(slot + ok_, hk + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
         !ok(cudaMemcpyAsync(slot + ov, hv + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
@@ -133,7 +138,7 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
       break;
     // compute chunk i on the caller's stream (heads h0 .. h0+nh-1 as one batch)
     if (!ok(cudaStreamWaitEvent(s, pipe->in_done[i], 0))) break;
-    if (i >= 2 && !ok(cudaStreamWaitEvent(s, pipe->out_done[i - 2], 0))) break;
+    if (i >= fa::kSlots && !ok(cudaStreamWaitEvent(s, pipe->out_done[i - fa::kSlots], 0))) break;
     const int r = fa_fwd(slot + oq, slot + ok_, slot + ov, slot + oo,
                          lse != nullptr ? reinterpret_cast<float*>(slot + ol) : nullptr, 1, int(nh), Lq, Lk,
                          D, scale, causal, s);
@@ -162,9 +167,15 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
     cudaStreamSynchronize(s);
   }
   const bool freed = fa::workspace_free(ws, s) == FA_OK;
-  const bool synced = cudaStreamSynchronize(s) == cudaSuccess;
   if (st != FA_OK) return st;
-  return freed && synced ? FA_OK : FA_ERR_CUDA;
+  return freed ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int Lq, int Lk, int D, float scale, int causal, void* stream) {
+  const int st = fa_fwd_host_async(q, k, v, o, lse, B, H, Lq, Lk, D, scale, causal, stream);
+  if (st != FA_OK) return st;
+  return cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // extern "C"

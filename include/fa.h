@@ -245,14 +245,25 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
  * consecutive heads (at least 8 MiB of copies each, fa_host_num_chunks), and
  * the copies of one chunk overlap the computation of the next: copy-in,
  * compute and copy-out run on three streams (two internal copy streams and
- * `stream`, which carries the computation), ordered by events, with two
+ * `stream`, which carries the computation), ordered by events, with three
  * chunks of device memory from the library's pool.  Same argument rules as
  * fa_fwd (lse may be NULL; host pointers have no alignment rule).  The call
- * returns after the outputs are in host memory.  Calls on one device are
- * serialised (they share the copy streams).
+ * returns after the outputs are in host memory.  Calls on one device share
+ * the two copy streams (queueing a call takes a per-device lock).
  */
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Lq, int Lk, int D, float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_host_async - fa_fwd_host without the final synchronisation: returns
+ * once the copies and kernels are queued; the outputs are in host memory when
+ * `stream` has reached the point after this call (cudaStreamSynchronize, or an
+ * event recorded on it).  The host buffers must stay valid until then.  The
+ * copy-in of a following call runs while this call computes, so a sequence of
+ * calls followed by one synchronisation overlaps their copies and kernels.
+ */
+int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Lq, int Lk, int D, float scale, int causal, void* stream);
 
 /* fa_host_num_chunks - the number of head chunks fa_fwd_host uses for BH heads
  * of bytes_per_head copied bytes each: min(8, BH, BH * bytes_per_head / 8 MiB),
@@ -263,7 +274,7 @@ int fa_host_num_chunks(long long BH, long long bytes_per_head);
 /* fa_abi_version - (major << 16) | minor of this header's ABI. */
 int fa_abi_version(void);
 
-#define FA_ABI_VERSION ((1 << 16) | 5)
+#define FA_ABI_VERSION ((1 << 16) | 6)
 
 #ifdef __cplusplus
 }

@@ -30,7 +30,8 @@ def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
               "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows",
-              "fa_bwd", "fa_fwd_dropout", "fa_fwd_host", "fa_host_num_chunks"):
+              "fa_bwd", "fa_fwd_dropout", "fa_fwd_host", "fa_host_num_chunks",
+              "fa_fwd_host_async"):
         assert n in names
 
 
@@ -42,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.fa_abi_version() == (1 << 16) | 5
+    assert lib.fa_abi_version() == (1 << 16) | 6
 
 
 def test_strerror_covers_every_status(lib):
@@ -272,3 +273,8 @@ def test_host_chunk_rule(lib, BH, per, expect):
     if BH > 0 and per > 0:
         hc = -(-BH // n)
         assert (n - 1) * hc < BH <= n * hc
+
+
+def test_host_async_entry_rejects_bad_arguments_on_host(lib):
+    assert lib.fa_fwd_host_async(None, A, A, A, A, 1, 1, 128, 128, 128, 0.1, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_host_async(A, A, A, A, A, 1, 1, 128, 128, 96, 0.1, 0, None) == fa.FA_ERR_UNSUPPORTED

@@ -85,3 +85,20 @@ def test_repeated_calls_reuse_the_pipeline():
     q, k, v = _host_inputs(2, 8, 2048, 2048, 64, seed=9)
     outs = [fa.forward_host(q, k, v)[0].clone() for _ in range(3)]
     assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_async_calls_queued_back_to_back():
+    """Several problems queued with sync=False and one synchronisation: each
+    output equals the device forward of its own inputs."""
+    shapes = [(2, 8, 2048, 2048, 64, False), (1, 4, 1000, 1000, 128, True), (4, 8, 4096, 4096, 64, False),
+              (1, 2, 1, 5000, 128, False)]
+    probs = [(_host_inputs(*sh[:5], seed=20 + i), sh) for i, sh in enumerate(shapes)]
+    outs = [fa.forward_host(q, k, v, causal=sh[5], sync=False) for (q, k, v), sh in probs]
+    torch.cuda.current_stream().synchronize()
+    for ((q, k, v), sh), (oh, lh) in zip(probs, outs):
+        od, ld = fa.forward(q.cuda(), k.cuda(), v.cuda(), causal=sh[5])
+        if sh[2] == 1:
+            assert float((oh.float() - od.cpu().float()).abs().max()) <= 4e-3
+            assert float((lh - ld.cpu()).abs().max()) <= 1e-5
+        else:
+            assert torch.equal(oh, od.cpu()) and torch.equal(lh, ld.cpu())
