@@ -209,7 +209,8 @@ def run_ours(args, rank, world):
     for i, w in enumerate(ws):
         ts = [times[s * n + i] for s in range(args.steps)]
         ms = statistics.median(ts)
-        per_len[str(w.Lq)] = {"ms": round(ms, 5), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2)}
+        per_len[str(w.Lq)] = {"ms": round(ms, 5), "tflops": round(w.flops / (ms * 1e-3) / 1e12, 2),
+                              "GB/s": round(w.bytes / (ms * 1e-3) / 1e9, 1)}
 
     # ---- e2e: the same sweep through the host-buffer API
     host = [(w, *(t.cpu().pin_memory() for t in (q, k, v)),
@@ -278,14 +279,15 @@ def per_config(args, fa, flush, dev, peaks, check):
     import torch
     from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
     out = {}
-    for name, reps in (("mha_l256_d64", 20), ("causal_l8k_d128", 10),
-                       ("causal_l64k_d128", 3), ("decode_l128k_d128", 5)):
+    # median of >= 20 timed launches (>= 5 for the 22 ms long-context one), 3 warm-ups
+    for name, reps in (("mha_l256_d64", 20), ("causal_l8k_d128", 20),
+                       ("causal_l64k_d128", 5), ("decode_l128k_d128", 20)):
         w = WORKLOADS[name]
         q, k, v = make_inputs(w, dev)
         o = torch.empty((w.B, w.H, w.Lq, w.D), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((w.B, w.H, w.Lq), dtype=torch.float32, device=dev)
         call = lambda: fa.forward(q, k, v, causal=w.causal, out=o, lse=lse)
-        _time_launches([call], flush, 2)
+        _time_launches([call], flush, 3)
         ts = _time_launches([call], flush, reps)
         check()
         ms = statistics.median(ts)
@@ -302,6 +304,8 @@ def per_config(args, fa, flush, dev, peaks, check):
             tr = (measured_traffic("fa_prefill_kernel<128>/causal_l8k_d128", PREFILL_SOURCES)
                   if name == "causal_l8k_d128" else None)
             entry.update({"TFLOPS": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+                          "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),
+                          "GB/s": round(w.bytes / (ms * 1e-3) / 1e9, 1),
                           "launches": 1, "algorithmic_bytes": w.bytes, "traffic": tr})
         out[name] = entry
         del q, k, v, o, lse
@@ -461,10 +465,30 @@ def _oracle_sample(max_seconds, per_len_rows=None, max_rounds=None):
                           " per head (numpy fp64, BLAS threads = all host cores)")
 
 
+def cpu_model():
+    """The host CPU's model as the OS reports it (x86: 'model name'; Arm:
+    implementer and part numbers), else the machine type."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model name"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    return line.split(":", 1)[1].strip()
+        impl = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU implementer")]
+        part = [l.split(":", 1)[1].strip() for l in info.splitlines() if l.startswith("CPU part")]
+        if impl and part:
+            return f"Arm implementer {impl[0]} part {part[0]}"
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def cpu_baseline(seconds):
     flops, spent, desc = _oracle_sample(seconds)
     return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOPS",
-            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "cores": len(os.sched_getaffinity(0)), "cpu": cpu_model(), "kind": "oracle",
             "sample": desc,
             "seconds": round(spent, 2)}
 
@@ -488,7 +512,7 @@ def run_reference(args, rank, world):
             "config": {"workload": "sweep_d64: non-causal MHA B=4 H=8 D=64, Lq=Lk in 64..8192",
                        "sample": desc},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
-                             "kind": "oracle", "sample": desc},
+                             "cpu": cpu_model(), "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
