@@ -5,16 +5,19 @@
 // consecutive heads (the [B, H, L, D] layout keeps a chunk contiguous) and run
 // as a three-stage pipeline on three streams: the copies of chunk i+1 into the
 // device run while chunk i is computed on the caller's stream and the output of
-// chunk i-1 is copied back.  The two copy directions use separate copy engines,
-// and the device memory holds three chunks (from the library's workspace
-// pool).  Events order the stages:
-//   copy-in i    after compute i-3 (its input slot is free)
-//   compute i    after copy-in i and after copy-out i-3 (its output slot is free)
-//   copy-out i   after compute i
+// chunk i-1 is copied back.  The two copy directions use separate copy engines.
+// The device memory is a ring of three chunk slots kept per device across
+// calls, and chunks are numbered across calls, so that chunk g uses slot g mod
+// 3 whichever call it belongs to.  Events (one per slot and stage) order the
+// stages:
+//   copy-in g    after compute g-3 (its input slot is free)
+//   compute g    after copy-in g and after copy-out g-3 (its output slot is free)
+//   copy-out g   after compute g
 // fa_fwd_host returns when the outputs are in host memory; fa_fwd_host_async
 // returns once the work is queued (complete when `stream` reaches that point),
-// so that the copy-in of the next call runs while this one computes: the
-// workspace is taken on the copy-in stream, not behind the caller's stream.
+// so that the copy-in of the next call runs while this one computes.  The
+// ring grows (after the work in flight has finished) when a call needs larger
+// slots.
 #include "fa.h"
 #include "fa_internal.h"
 
@@ -27,18 +30,20 @@ namespace fa {
 namespace {
 
 constexpr int kMaxChunks = 8;
-constexpr int kSlots = 3;      // chunks of device memory in flight
+constexpr int kSlots = 3;      // chunk slots of device memory
 constexpr long long kMinChunkBytes = 8ll << 20;   // below this a chunk's copy is latency-bound
 constexpr int kMaxDevices = 64;
 
-// per-device copy streams and events, created once; calls on one device are
-// serialised by a mutex because they share them
+// per-device copy streams, events and slot ring, created once; queueing a
+// call takes the mutex because calls share them
 struct HostPipe {
   std::mutex mu;
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t start = nullptr;
-  cudaEvent_t in_done[kMaxChunks] = {}, comp_done[kMaxChunks] = {}, out_done[kMaxChunks] = {};
+  cudaEvent_t in_done[kSlots] = {}, comp_done[kSlots] = {}, out_done[kSlots] = {};
+  uint8_t* ring = nullptr;          // kSlots slots of slot_cap bytes
+  size_t slot_cap = 0;
+  unsigned long long next = 0;      // number of the next chunk
 };
 
 HostPipe* host_pipe(int dev) {
@@ -51,8 +56,7 @@ bool init_pipe(HostPipe& p) {
   if (p.ready) return true;
   if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
-  if (cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) != cudaSuccess) return false;
-  for (int i = 0; i < kMaxChunks; ++i)
+  for (int i = 0; i < kSlots; ++i)
     if (cudaEventCreateWithFlags(&p.in_done[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.out_done[i], cudaEventDisableTiming) != cudaSuccess)
@@ -62,6 +66,24 @@ bool init_pipe(HostPipe& p) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// a ring whose slots hold `slot_bytes`; a larger one is allocated only after
+// every chunk in flight has finished with the old one
+bool ensure_ring(HostPipe& p, size_t slot_bytes) {
+  if (p.ring != nullptr && p.slot_cap >= slot_bytes) return true;
+  for (int i = 0; i < kSlots; ++i)
+    if (cudaEventSynchronize(p.out_done[i]) != cudaSuccess || cudaEventSynchronize(p.comp_done[i]) != cudaSuccess)
+      return false;
+  if (cudaStreamSynchronize(p.h2d) != cudaSuccess || cudaStreamSynchronize(p.d2h) != cudaSuccess) return false;
+  if (p.ring != nullptr && cudaFree(p.ring) != cudaSuccess) return false;
+  p.ring = nullptr;
+  p.slot_cap = 0;
+  void* mem = nullptr;
+  if (cudaMalloc(&mem, kSlots * slot_bytes) != cudaSuccess) return false;
+  p.ring = static_cast<uint8_t*>(mem);
+  p.slot_cap = slot_bytes;
+  return true;
+}
 
 }  // namespace
 }  // namespace fa
@@ -96,7 +118,6 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
   const size_t oq = 0, ok_ = fa::round_up(oq + hc * qb, 256), ov = fa::round_up(ok_ + hc * kb, 256),
                oo = fa::round_up(ov + hc * kb, 256), ol = fa::round_up(oo + hc * qb, 256),
                slot_bytes = fa::round_up(ol + hc * lb, 256);
-  const int slots = std::min(n, fa::kSlots);
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -106,11 +127,7 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
   std::lock_guard<std::mutex> lock(pipe->mu);
   if (!fa::init_pipe(*pipe)) return FA_ERR_CUDA;
 
-  // the workspace is ordered on the copy-in stream: the other two streams
-  // start after the allocation point
-  void* ws = nullptr;
-  if (fa::workspace_alloc(&ws, slots * slot_bytes, pipe->h2d) != FA_OK) return FA_ERR_CUDA;
-  uint8_t* base = static_cast<uint8_t*>(ws);
+  if (!fa::ensure_ring(*pipe, slot_bytes)) return FA_ERR_CUDA;
   const uint8_t* hq = static_cast<const uint8_t*>(q);
   const uint8_t* hk = static_cast<const uint8_t*>(k);
   const uint8_t* hv = static_cast<const uint8_t*>(v);
@@ -122,23 +139,22 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
     if (e != cudaSuccess && st == FA_OK) st = FA_ERR_CUDA;
     return st == FA_OK;
   };
-  if (ok(cudaEventRecord(pipe->start, pipe->h2d))) {
-    ok(cudaStreamWaitEvent(s, pipe->start, 0));
-    ok(cudaStreamWaitEvent(pipe->d2h, pipe->start, 0));
-  }
   for (int i = 0; i < n && st == FA_OK; ++i) {
     const long long h0 = i * hc, nh = std::min(hc, BH - h0);
-    uint8_t* slot = base + size_t(i % fa::kSlots) * slot_bytes;
-    // copy-in of chunk i, once compute i-3 has released the slot's inputs
-    if (i >= fa::kSlots && !ok(cudaStreamWaitEvent(pipe->h2d, pipe->comp_done[i - fa::kSlots], 0))) break;
+    const int e = int(pipe->next++ % fa::kSlots);   // slot of this chunk, and of chunk - 3
+    uint8_t* slot = pipe->ring + size_t(e) * pipe->slot_cap;
+    // copy-in once compute of chunk - 3 (of this or an earlier call) has
+    // released the slot's inputs (an event never recorded is complete)
+    if (!ok(cudaStreamWaitEvent(pipe->h2d, pipe->comp_done[e], 0))) break;
     if (!ok(cudaMemcpyAsync(slot + oq, hq + h0 * qb, nh * qb, cudaMemcpyHostToDevice, pipe->h2d)) ||
         !ok(cudaMemcpyAsync(slot + ok_, hk + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
         !ok(cudaMemcpyAsync(slot + ov, hv + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
-        !ok(cudaEventRecord(pipe->in_done[i], pipe->h2d)))
+        !ok(cudaEventRecord(pipe->in_done[e], pipe->h2d)))
       break;
-    // compute chunk i on the caller's stream (heads h0 .. h0+nh-1 as one batch)
-    if (!ok(cudaStreamWaitEvent(s, pipe->in_done[i], 0))) break;
-    if (i >= fa::kSlots && !ok(cudaStreamWaitEvent(s, pipe->out_done[i - fa::kSlots], 0))) break;
+    // compute on the caller's stream (heads h0 .. h0+nh-1 as one batch), once
+    // the copy-out of chunk - 3 has read the slot's outputs
+    if (!ok(cudaStreamWaitEvent(s, pipe->in_done[e], 0))) break;
+    if (!ok(cudaStreamWaitEvent(s, pipe->out_done[e], 0))) break;
     const int r = fa_fwd(slot + oq, slot + ok_, slot + ov, slot + oo,
                          lse != nullptr ? reinterpret_cast<float*>(slot + ol) : nullptr, 1, int(nh), Lq, Lk,
                          D, scale, causal, s);
@@ -146,29 +162,25 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
       st = r;
       break;
     }
-    if (!ok(cudaEventRecord(pipe->comp_done[i], s))) break;
-    // copy-out of chunk i
-    if (!ok(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[i], 0))) break;
+    if (!ok(cudaEventRecord(pipe->comp_done[e], s))) break;
+    // copy-out
+    if (!ok(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[e], 0))) break;
     if (!ok(cudaMemcpyAsync(ho + h0 * qb, slot + oo, nh * qb, cudaMemcpyDeviceToHost, pipe->d2h))) break;
     if (lse != nullptr && !ok(cudaMemcpyAsync(hl + h0 * lb, slot + ol, nh * lb, cudaMemcpyDeviceToHost, pipe->d2h)))
       break;
-    if (!ok(cudaEventRecord(pipe->out_done[i], pipe->d2h))) break;
+    if (!ok(cudaEventRecord(pipe->out_done[e], pipe->d2h))) break;
   }
-  // every copy has finished before the workspace goes back to the pool: on
-  // success the caller's stream waits for the last copy-out; on an error all
-  // three streams are drained first
   if (st == FA_OK) {
-    // copy-outs run in order on one stream, and every copy-in finished before
-    // the last compute started
-    ok(cudaStreamWaitEvent(s, pipe->out_done[n - 1], 0));
+    // the caller's stream reaches the end of this call once the last
+    // copy-out has landed (copy-outs run in order on one stream)
+    ok(cudaStreamWaitEvent(s, pipe->out_done[(pipe->next - 1) % fa::kSlots], 0));
   } else {
+    // a failed call leaves nothing in flight
     cudaStreamSynchronize(pipe->h2d);
     cudaStreamSynchronize(pipe->d2h);
     cudaStreamSynchronize(s);
   }
-  const bool freed = fa::workspace_free(ws, s) == FA_OK;
-  if (st != FA_OK) return st;
-  return freed ? FA_OK : FA_ERR_CUDA;
+  return st;
 }
 
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
