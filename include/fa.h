@@ -245,8 +245,9 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
  * consecutive heads (at least 8 MiB of copies each, fa_host_num_chunks), and
  * the copies of one chunk overlap the computation of the next: copy-in,
  * compute and copy-out run on three streams (two internal copy streams and
- * `stream`, which carries the computation), ordered by events, with three
- * chunks of device memory from the library's pool.  Same argument rules as
+ * `stream`, which carries the computation), ordered by events, over a ring of
+ * three chunk slots of device memory the library keeps per device (grown when
+ * a call needs larger slots, after the work in flight).  Same argument rules as
  * fa_fwd (lse may be NULL; host pointers have no alignment rule).  The call
  * returns after the outputs are in host memory.  Calls on one device share
  * the two copy streams (queueing a call takes a per-device lock).
