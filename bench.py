@@ -272,6 +272,8 @@ def run_ours(args, rank, world):
         result["per_config"] = per_config(args, fa, flush, dev, peaks, check)
     if rank == 0 and world == 1 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        if args.oracle_configs:
+            result["cpu_baseline"]["per_config"] = oracle_per_config()
     return result
 
 
@@ -465,6 +467,43 @@ def _oracle_sample(max_seconds, per_len_rows=None, max_rounds=None):
                           " per head (numpy fp64, BLAS threads = all host cores)")
 
 
+def oracle_per_config(seconds_each=5.0):
+    """The oracle's rate on bounded samples of the other workloads (on the
+    host cores, after the GPU part): the L = 256 config whole; whole heads of
+    the causal 8K config; the long-context config's sampled rows of its first
+    heads; whole heads of the 128K decode config.  Each sample stops after
+    about `seconds_each` of oracle time.  Rates are over the flops of the rows
+    computed (causal: the visible keys only), or the K/V bytes for decode."""
+    import numpy as np
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs, sample_rows
+    from oracle.naive import attention_head, to_f64
+
+    out = {}
+    for name in ("mha_l256_d64", "causal_l8k_d128", "causal_l64k_d128", "decode_l128k_d128"):
+        w = WORKLOADS[name]
+        q, k, v = make_inputs(w, "cpu", batches=range(1))   # batch 0 only (bounded host memory)
+        picked = sample_rows(w) if name == "causal_l64k_d128" else None
+        flops = nbytes = spent = 0.0
+        heads = 0
+        for h in range(w.H):
+            qh, kh, vh = to_f64(q[0, h]), to_f64(k[0, h]), to_f64(v[0, h])
+            rows = picked[h].numpy() if picked is not None else np.arange(w.Lq)
+            t0 = time.perf_counter()
+            attention_head(qh, kh, vh, w.scale, causal=w.causal, rows=rows)
+            spent += time.perf_counter() - t0
+            keys = (rows + 1) if w.causal else np.full(rows.shape, w.Lk)
+            flops += 4.0 * float(keys.sum()) * w.D
+            nbytes += 4.0 * w.Lk * w.D
+            heads += 1
+            if spent > seconds_each:
+                break
+        entry = {"heads": heads, "seconds": round(spent, 2), "GFLOP/s": round(flops / spent / 1e9, 3)}
+        if w.Lq == 1:
+            entry["GB/s"] = round(nbytes / spent / 1e9, 3)
+        out[name] = entry
+    return out
+
+
 def cpu_model():
     """The host CPU's model as the OS reports it (x86: 'model name'; Arm:
     implementer and part numbers), else the machine type."""
@@ -576,6 +615,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config section")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="also time the oracle on bounded samples of the other workloads (~20 s)")
     ap.add_argument("--profile-case", default=None, help="run one workload (for ncu captures)")
     ap.add_argument("--profile-batch", type=int, default=0, help="batch override for --profile-case")
     ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward", "paged", "softmax"],
