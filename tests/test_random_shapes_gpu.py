@@ -1,7 +1,9 @@
-"""Seeded random shapes through the C ABI against the fp64 oracle, element by
+"""Seeded random shapes through the C ABI against the fp64 oracles, element by
 element: the forward (head dims 64 and 128, causal or not, lengths that are
 and are not multiples of the 128-row tiles, Lq != Lk, a custom scale, and
-logits of several magnitudes) and the backward.  The shapes come from one
+logits of several magnitudes), the backward, the forward with dropout
+(random p, 64-bit seeds and offsets) and the paged decode (random page
+sizes, lengths, empty sequences, page tables).  The shapes come from one
 fixed generator, so a failure names a reproducible case; they complement the
 hand-picked edge shapes of the other parity tests."""
 import math
@@ -84,3 +86,76 @@ def test_backward_random_shape(i, B, H, Lq, Lk, D, causal):
         err = float(np.abs(got.float().cpu().numpy().astype(np.float64) - ref).max())
         mag = float(np.abs(ref).max())
         assert err <= 2e-2 * max(1.0, mag), f"case {i} {name}: {err:.3e} (max |ref| {mag:.3e})"
+
+
+def _dropout_cases(n=10, seed=31):
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        D = rng.choice((64, 128))
+        causal = rng.random() < 0.5
+        Lq = rng.randint(1, 600)
+        Lk = Lq if causal else rng.randint(1, 600)
+        if causal and Lq == 1:
+            Lq = Lk = 2
+        p = rng.choice((0.0, 0.05, 0.2, 0.5, 0.9))
+        seed64 = rng.getrandbits(64)
+        offset = rng.getrandbits(32)
+        cases.append((i, rng.choice((1, 2)), rng.choice((1, 3)), Lq, Lk, D, causal, p, seed64, offset))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,H,Lq,Lk,D,causal,p,seed64,offset", _dropout_cases())
+def test_dropout_random_shape(i, B, H, Lq, Lk, D, causal, p, seed64, offset):
+    from oracle import dropout as od
+    from oracle.naive import to_f64
+    g = torch.Generator().manual_seed(7000 + i)
+    q = torch.randn(B, H, Lq, D, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(B, H, Lk, D, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(B, H, Lk, D, generator=g).to(torch.bfloat16).cuda()
+    o, lse = fa.forward_dropout(q, k, v, p, seed64, offset, causal=causal)
+    st, site = fa.last_device_error()
+    assert st == fa.FA_OK, (st, site)
+    t = od.drop_threshold(p)
+    scale = 1.0 / math.sqrt(D)
+    for b in range(B):
+        for h in range(H):
+            ro, rl, _ = od.attention_dropout_rows(to_f64(q[b, h].cpu()), to_f64(k[b, h].cpu()),
+                                                  to_f64(v[b, h].cpu()), scale, causal, np.arange(Lq),
+                                                  b * H + h, p, seed64, offset)
+            d_o = float(np.abs(to_f64(o[b, h].cpu()) - ro).max())
+            d_l = float(np.abs(to_f64(lse[b, h].cpu()) - rl).max())
+            assert d_o <= ATOL_O * 256 / (256 - t), f"case {i}: max |dO| = {d_o:.3e}"
+            assert d_l <= ATOL_LSE, f"case {i}: max |dLSE| = {d_l:.3e}"
+
+
+def _paged_cases(n=6, seed=53):
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        page = rng.choice((1, 4, 16, 64, 256))
+        max_pages = rng.randint(1, max(1, 3000 // page))
+        B = rng.randint(1, 5)
+        lengths = tuple(rng.randint(0, max_pages * page) for _ in range(B))
+        cases.append((i, B, rng.choice((1, 4)), rng.choice((64, 128)), page, max_pages, lengths))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,H,D,page,max_pages,lengths", _paged_cases())
+def test_paged_random_shape(i, B, H, D, page, max_pages, lengths):
+    from exact_attention_03_gb300.inputs import PagedWorkload, make_paged_inputs
+    from oracle.paged import decode_paged as oracle_paged
+    w = PagedWorkload(f"r{i}", B, H, D, page, max_pages * page, 300 + i, lengths=lengths)
+    q, kc, vc, bt, lens = make_paged_inputs(w, "cuda")
+    o, lse = fa.decode_paged(q, kc, vc, bt, lens, scale=w.scale)
+    st, site = fa.last_device_error()
+    assert st == fa.FA_OK, (st, site)
+    ro, rl = oracle_paged(q.cpu(), kc.cpu(), vc.cpu(), bt.cpu(), lens.cpu(), w.scale)
+    go = o.float().cpu().numpy().astype(np.float64)
+    gl = lse.cpu().numpy().astype(np.float64)
+    empty = np.isneginf(rl)
+    assert np.array_equal(np.isneginf(gl), empty)
+    assert np.all(go[empty] == 0)
+    assert float(np.abs(go - ro).max()) <= ATOL_O
+    if (~empty).any():
+        assert float(np.abs(gl[~empty] - rl[~empty]).max()) <= ATOL_LSE
