@@ -3,21 +3,24 @@
 //
 // Heads are independent problems, so one call is split into chunks of
 // consecutive heads (the [B, H, L, D] layout keeps a chunk contiguous) and run
-// as a three-stage pipeline on three streams: the copies of chunk i+1 into the
-// device run while chunk i is computed on the caller's stream and the output of
-// chunk i-1 is copied back.  The two copy directions use separate copy engines.
-// The device memory is a ring of three chunk slots kept per device across
-// calls, and chunks are numbered across calls, so that chunk g uses slot g mod
-// 3 whichever call it belongs to.  Events (one per slot and stage) order the
-// stages:
+// as a three-stage pipeline: the copies of chunk i+1 into the device run while
+// chunk i is computed and the output of chunk i-1 is copied back.  The two
+// copy directions use separate copy engines.  Chunks are computed on two
+// streams in turn, so that the kernel of one chunk fills the SMs the previous
+// chunk's kernel leaves idle (a chunk of a few heads is often less than one
+// full wave of CTAs).  The device memory is a ring of three chunk slots kept
+// per device across calls, and chunks are numbered across calls, so that
+// chunk g uses slot g mod 3 whichever call it belongs to.  Events (one per
+// slot and stage) order the stages:
 //   copy-in g    after compute g-3 (its input slot is free)
 //   compute g    after copy-in g and after copy-out g-3 (its output slot is free)
 //   copy-out g   after compute g
-// fa_fwd_host returns when the outputs are in host memory; fa_fwd_host_async
-// returns once the work is queued (complete when `stream` reaches that point),
-// so that the copy-in of the next call runs while this one computes.  The
-// ring grows (after the work in flight has finished) when a call needs larger
-// slots.
+// The caller's stream waits for the last copy-out (copy-outs run in order on
+// one stream).  fa_fwd_host returns when the outputs are in host memory;
+// fa_fwd_host_async returns once the work is queued (complete when `stream`
+// reaches that point), so that the copy-in of the next call runs while this
+// call computes.  The ring grows (after the work in flight has finished) when
+// a call needs larger slots.
 #include "fa.h"
 #include "fa_internal.h"
 
@@ -31,6 +34,7 @@ namespace {
 
 constexpr int kMaxChunks = 8;
 constexpr int kSlots = 3;      // chunk slots of device memory
+constexpr int kCompStreams = 2;
 constexpr long long kMinChunkBytes = 8ll << 20;   // below this a chunk's copy is latency-bound
 constexpr int kMaxDevices = 64;
 
@@ -39,7 +43,7 @@ constexpr int kMaxDevices = 64;
 struct HostPipe {
   std::mutex mu;
   bool ready = false;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp[kCompStreams] = {};
   cudaEvent_t in_done[kSlots] = {}, comp_done[kSlots] = {}, out_done[kSlots] = {};
   uint8_t* ring = nullptr;          // kSlots slots of slot_cap bytes
   size_t slot_cap = 0;
@@ -56,6 +60,8 @@ bool init_pipe(HostPipe& p) {
   if (p.ready) return true;
   if (cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking) != cudaSuccess) return false;
   if (cudaStreamCreateWithFlags(&p.d2h, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (int i = 0; i < kCompStreams; ++i)
+    if (cudaStreamCreateWithFlags(&p.comp[i], cudaStreamNonBlocking) != cudaSuccess) return false;
   for (int i = 0; i < kSlots; ++i)
     if (cudaEventCreateWithFlags(&p.in_done[i], cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&p.comp_done[i], cudaEventDisableTiming) != cudaSuccess ||
@@ -75,6 +81,8 @@ bool ensure_ring(HostPipe& p, size_t slot_bytes) {
     if (cudaEventSynchronize(p.out_done[i]) != cudaSuccess || cudaEventSynchronize(p.comp_done[i]) != cudaSuccess)
       return false;
   if (cudaStreamSynchronize(p.h2d) != cudaSuccess || cudaStreamSynchronize(p.d2h) != cudaSuccess) return false;
+  for (int i = 0; i < kCompStreams; ++i)
+    if (cudaStreamSynchronize(p.comp[i]) != cudaSuccess) return false;
   if (p.ring != nullptr && cudaFree(p.ring) != cudaSuccess) return false;
   p.ring = nullptr;
   p.slot_cap = 0;
@@ -151,18 +159,19 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
         !ok(cudaMemcpyAsync(slot + ov, hv + h0 * kb, nh * kb, cudaMemcpyHostToDevice, pipe->h2d)) ||
         !ok(cudaEventRecord(pipe->in_done[e], pipe->h2d)))
       break;
-    // compute on the caller's stream (heads h0 .. h0+nh-1 as one batch), once
-    // the copy-out of chunk - 3 has read the slot's outputs
-    if (!ok(cudaStreamWaitEvent(s, pipe->in_done[e], 0))) break;
-    if (!ok(cudaStreamWaitEvent(s, pipe->out_done[e], 0))) break;
+    // compute (heads h0 .. h0+nh-1 as one batch) on the compute streams in
+    // turn, once the copy-out of chunk - 3 has read the slot's outputs
+    cudaStream_t cs = pipe->comp[(pipe->next - 1) % fa::kCompStreams];
+    if (!ok(cudaStreamWaitEvent(cs, pipe->in_done[e], 0))) break;
+    if (!ok(cudaStreamWaitEvent(cs, pipe->out_done[e], 0))) break;
     const int r = fa_fwd(slot + oq, slot + ok_, slot + ov, slot + oo,
                          lse != nullptr ? reinterpret_cast<float*>(slot + ol) : nullptr, 1, int(nh), Lq, Lk,
-                         D, scale, causal, s);
+                         D, scale, causal, cs);
     if (r != FA_OK) {
       st = r;
       break;
     }
-    if (!ok(cudaEventRecord(pipe->comp_done[e], s))) break;
+    if (!ok(cudaEventRecord(pipe->comp_done[e], cs))) break;
     // copy-out
     if (!ok(cudaStreamWaitEvent(pipe->d2h, pipe->comp_done[e], 0))) break;
     if (!ok(cudaMemcpyAsync(ho + h0 * qb, slot + oo, nh * qb, cudaMemcpyDeviceToHost, pipe->d2h))) break;
@@ -177,6 +186,7 @@ int fa_fwd_host_async(const void* q, const void* k, const void* v, void* o, floa
   } else {
     // a failed call leaves nothing in flight
     cudaStreamSynchronize(pipe->h2d);
+    for (int i = 0; i < fa::kCompStreams; ++i) cudaStreamSynchronize(pipe->comp[i]);
     cudaStreamSynchronize(pipe->d2h);
     cudaStreamSynchronize(s);
   }

@@ -244,13 +244,16 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
  * pageable memory works, slower).  The heads are split into up to 8 chunks of
  * consecutive heads (at least 8 MiB of copies each, fa_host_num_chunks), and
  * the copies of one chunk overlap the computation of the next: copy-in,
- * compute and copy-out run on three streams (two internal copy streams and
- * `stream`, which carries the computation), ordered by events, over a ring of
+ * compute and copy-out run on internal streams (one per copy direction, and
+ * two compute streams taken in turn, so that one chunk's kernel fills the SMs
+ * the previous chunk's kernel leaves idle), ordered by events, over a ring of
  * three chunk slots of device memory the library keeps per device (grown when
- * a call needs larger slots, after the work in flight).  Same argument rules as
- * fa_fwd (lse may be NULL; host pointers have no alignment rule).  The call
- * returns after the outputs are in host memory.  Calls on one device share
- * the two copy streams (queueing a call takes a per-device lock).
+ * a call needs larger slots, after the work in flight); `stream` waits for the
+ * last copy-out.  The inputs are read as they are when the call is made (the
+ * copy-in is not ordered after work queued earlier on `stream`).  Same
+ * argument rules as fa_fwd (lse may be NULL; host pointers have no alignment
+ * rule).  The call returns after the outputs are in host memory.  Calls on one
+ * device share the internal streams (queueing a call takes a per-device lock).
  */
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int Lq, int Lk, int D, float scale, int causal, void* stream);
