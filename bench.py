@@ -524,12 +524,56 @@ def cpu_model():
     return platform.machine()
 
 
+def _oracle_l256_rate():
+    """The oracle over the whole L = 256 config (B4 H8 D64, non-causal, every
+    row of every head) in this process, repeated until it has run ~1 s;
+    returns its rate."""
+    import numpy as np
+    from exact_attention_03_gb300.inputs import WORKLOADS, make_inputs
+    from oracle.naive import attention_head, to_f64
+
+    w = WORKLOADS["mha_l256_d64"]
+    q, k, v = make_inputs(w, "cpu")
+    spent = 0.0
+    rounds = 0
+    while rounds == 0 or spent < 1.0:
+        for b in range(w.B):
+            for h in range(w.H):
+                qh, kh, vh = to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h])
+                t0 = time.perf_counter()
+                attention_head(qh, kh, vh, w.scale, causal=w.causal, rows=np.arange(w.Lq))
+                spent += time.perf_counter() - t0
+        rounds += 1
+    return {"GFLOP/s": round(rounds * w.flops / spent / 1e9, 3), "seconds": round(spent, 3),
+            "rounds": rounds}
+
+
+def oracle_l256_one_core():
+    """The same on ONE host core: a child process (spawned, not forked) that
+    pins itself to one CPU, with the BLAS and OpenMP thread counts set to 1
+    before numpy loads."""
+    cpu = min(os.sched_getaffinity(0))
+    code = (f"import os; os.sched_setaffinity(0, {{{cpu}}}); import json, bench; "
+            "print(json.dumps(bench._oracle_l256_rate()))")
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1")
+    try:
+        out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                             text=True, timeout=600)
+        res = json.loads(out.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    res.update({"cores": 1, "workload": "mha_l256_d64 (B4 H8 L256 D64, all rows)"})
+    return res
+
+
 def cpu_baseline(seconds):
     flops, spent, desc = _oracle_sample(seconds)
     return {"value": round(flops / spent / 1e12, 6), "unit": "TFLOPS",
             "cores": len(os.sched_getaffinity(0)), "cpu": cpu_model(), "kind": "oracle",
             "sample": desc,
-            "seconds": round(spent, 2)}
+            "seconds": round(spent, 2),
+            "one_core_l256": oracle_l256_one_core()}
 
 
 def run_reference(args, rank, world):
