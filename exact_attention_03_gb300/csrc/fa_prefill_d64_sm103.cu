@@ -349,8 +349,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Until a row has a finite running maximum its first tile takes the
       // maximum before exponentiating; later tiles exponentiate against the
-      // running maximum and check the result afterwards (below).
-      const bool exact = __any_sync(0xffffffffu, m_run == -INFINITY);
+      // running maximum and check the result afterwards (below).  With dropout
+      // every tile takes the maximum first: the random bits already dominate
+      // the loop, and a recomputed tile would draw them twice.
+      const bool exact = DROP || __any_sync(0xffffffffu, m_run == -INFINITY);
       if (exact) {
         const float m_cand = fmaxf(m_run, row_max128(s) * c);
         resc = __any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2);
