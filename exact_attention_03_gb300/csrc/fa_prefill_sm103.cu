@@ -113,6 +113,23 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Two counters under one key, their rounds interleaved so that the two
+// independent multiply chains overlap; the same bits as two philox4x32_10
+// calls (philox.cuh).
+__device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
+    const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
+    const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
+    const uint32_t bhi1 = __umulhi(0xCD9E8D57u, b.z), blo1 = 0xCD9E8D57u * b.z;
+    a = make_uint4(ahi1 ^ a.y ^ k0, alo1, ahi0 ^ a.w ^ k1, alo0);
+    b = make_uint4(bhi1 ^ b.y ^ k0, blo1, bhi0 ^ b.w ^ k1, blo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
 template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -383,13 +400,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cb = 0; cb < 4; ++cb) {
         uint4 dw;          // dropout bits of the current 16 keys
         uint32_t keep4;    // keep bytes of the current 4 keys
+        uint4 dw2;         // bits of the block's second 16 keys (both drawn up front)
+        if constexpr (DROP) {
+          const uint32_t g16 = uint32_t(k0 + 32 * cb) >> 4;
+          dw = make_uint4(g16, uint32_t(qrow), uint32_t(bh), p.offset);
+          dw2 = make_uint4(g16 + 1u, uint32_t(qrow), uint32_t(bh), p.offset);
+          philox4x32_10_x2(dw, dw2, p.seed_lo, p.seed_hi);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if constexpr (DROP)
-            if ((i & 7) == 0)
-              dw = philox4x32_10(make_uint4(uint32_t(k0 + 32 * cb + 2 * i) >> 4, uint32_t(qrow), uint32_t(bh),
-                                            p.offset),
-                                 p.seed_lo, p.seed_hi);
+            if (i == 8) dw = dw2;
           const float2 x = __ffma2_rn(make_float2(s[32 * cb + 2 * i], s[32 * cb + 2 * i + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
