@@ -226,6 +226,10 @@ def run_ours(args, rank, world):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         flush.zero_()
+        # the host-buffer copies run on the library's own streams, which do
+        # not wait for `s`: let the flush finish first, so that no copy of
+        # the step starts before e0
+        torch.cuda.synchronize()
         e0.record(s)
         # the step's problems are queued back to back (each one's copies
         # overlap the previous one's kernels); the outputs are on the host
