@@ -8,10 +8,10 @@
 // exp(a_i - Amax) / S.  This file is that two-read softmax as an operation of
 // its own over the rows of a matrix:
 //
-//   read 1: every thread keeps (d, s) over the 4-element groups it reads
-//           (one rescale per group), then the pairs of a warp, and of the warps
-//           of a CTA, are merged with the same identity (d = max, s = s1
-//           exp(d1 - d) + s2 exp(d2 - d));
+//   read 1: every thread keeps (d, s) over the groups of 4 elements (16 in
+//           the one-warp-per-row kernel) it reads, one rescale per group; then
+//           the pairs of a warp, and of the warps of a CTA, are merged with the
+//           same identity (d = max, s = s1 exp(d1 - d) + s2 exp(d2 - d));
 //   read 2: y_i = exp(a_i - d) / s, written once.
 //
 // A row of up to kWarpCols columns is one warp's (8 rows per CTA); a longer row
@@ -57,12 +57,23 @@ __device__ __forceinline__ void merge(float& D, float& s, float D2, float s2) {
 }
 
 // read 1 over this thread's share of a row: vector loads when the row is
-// 16-byte aligned, scalar loads otherwise
+// 16-byte aligned, scalar loads otherwise; with UNROLL, four loads in flight
+// per thread and one rescale per 16 values (the one-warp-per-row kernel,
+// whose rows give each thread few loads)
+template <bool UNROLL>
 __device__ __forceinline__ void scan(const float* row, int cols, int t, int nt, float& d, float& s) {
   if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
     const int n4 = cols >> 2;
     const float4* r4 = reinterpret_cast<const float4*>(row);
-    for (int i = t; i < n4; i += nt) {
+    int i = t;
+    if constexpr (UNROLL)
+    for (; i + 3 * nt < n4; i += 4 * nt) {
+      const float4 a = __ldg(r4 + i), b = __ldg(r4 + i + nt), c = __ldg(r4 + i + 2 * nt),
+                   e = __ldg(r4 + i + 3 * nt);
+      const float v[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, e.x, e.y, e.z, e.w};
+      online_group(d, s, v, 16);
+    }
+    for (; i < n4; i += nt) {
       const float4 v4 = __ldg(r4 + i);
       const float v[4] = {v4.x, v4.y, v4.z, v4.w};
       online_group(d, s, v, 4);
@@ -77,6 +88,7 @@ __device__ __forceinline__ void scan(const float* row, int cols, int t, int nt, 
 }
 
 // read 2: y = 2^(a log2 e - D) / s (a row without any finite value gives 0)
+template <bool UNROLL>
 __device__ __forceinline__ void write_row(const float* row, float* out, int cols, int t, int nt,
                                           float D, float s) {
   const bool empty = !(s > 0.f);
@@ -86,11 +98,21 @@ __device__ __forceinline__ void write_row(const float* row, float* out, int cols
     const int n4 = cols >> 2;
     const float4* r4 = reinterpret_cast<const float4*>(row);
     float4* o4 = reinterpret_cast<float4*>(out);
-    for (int i = t; i < n4; i += nt) {
-      const float4 v = __ldg(r4 + i);
-      o4[i] = make_float4(ex2_approx(fmaf(v.x, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.y, kLog2e, -ds)) * inv,
-                          ex2_approx(fmaf(v.z, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.w, kLog2e, -ds)) * inv);
+    auto weights = [&](const float4 v) {
+      return make_float4(ex2_approx(fmaf(v.x, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.y, kLog2e, -ds)) * inv,
+                         ex2_approx(fmaf(v.z, kLog2e, -ds)) * inv, ex2_approx(fmaf(v.w, kLog2e, -ds)) * inv);
+    };
+    int i = t;
+    if constexpr (UNROLL)
+    for (; i + 3 * nt < n4; i += 4 * nt) {
+      const float4 a = __ldg(r4 + i), b = __ldg(r4 + i + nt), c = __ldg(r4 + i + 2 * nt),
+                   e = __ldg(r4 + i + 3 * nt);
+      o4[i] = weights(a);
+      o4[i + nt] = weights(b);
+      o4[i + 2 * nt] = weights(c);
+      o4[i + 3 * nt] = weights(e);
     }
+    for (; i < n4; i += nt) o4[i] = weights(__ldg(r4 + i));
     for (int i = (n4 << 2) + t; i < cols; i += nt) out[i] = ex2_approx(fmaf(row[i], kLog2e, -ds)) * inv;
   } else {
     for (int i = t; i < cols; i += nt) out[i] = ex2_approx(fmaf(__ldg(row + i), kLog2e, -ds)) * inv;
@@ -114,9 +136,9 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_warp(const float* x, fl
   for (long long r = (long long)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); r < rows; r += warps) {
     const float* row = x + r * cols;
     float d = -INFINITY, s = 0.f;
-    scan(row, cols, lane, 32, d, s);
+    scan<true>(row, cols, lane, 32, d, s);
     warp_merge(d, s);
-    write_row(row, y + r * cols, cols, lane, 32, d, s);
+    write_row<true>(row, y + r * cols, cols, lane, 32, d, s);
     if (lse != nullptr && lane == 0) lse[r] = (s > 0.f) ? (d + __log2f(s)) * kLn2 : -INFINITY;
   }
 }
@@ -129,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_cta(const float* x, flo
   for (long long r = blockIdx.x; r < rows; r += gridDim.x) {
     const float* row = x + r * cols;
     float d = -INFINITY, s = 0.f;
-    scan(row, cols, threadIdx.x, kThreads, d, s);
+    scan<false>(row, cols, threadIdx.x, kThreads, d, s);
     warp_merge(d, s);
     if (lane == 0) {
       sd[warp] = d;
@@ -140,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) softmax_rows_cta(const float* x, flo
     s = ss[0];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) merge(d, s, sd[w], ss[w]);
-    write_row(row, y + r * cols, cols, threadIdx.x, kThreads, d, s);
+    write_row<false>(row, y + r * cols, cols, threadIdx.x, kThreads, d, s);
     if (lse != nullptr && threadIdx.x == 0) lse[r] = (s > 0.f) ? (d + __log2f(s)) * kLn2 : -INFINITY;
     __syncthreads();  // sd/ss are rewritten for the next row
   }
