@@ -473,9 +473,10 @@ def _oracle_sample(max_seconds, per_len_rows=None, max_rounds=None):
 
 def oracle_per_config(seconds_each=5.0):
     """The oracle's rate on bounded samples of the other workloads (on the
-    host cores, after the GPU part): the L = 256 config whole; whole heads of
-    the causal 8K config; the long-context config's sampled rows of its first
-    heads; whole heads of the 128K decode config.  Each sample stops after
+    host cores, after the GPU part), all from batch entry 0: the L = 256
+    config's 8 heads; whole heads of the causal 8K config; the long-context
+    config's sampled rows of its first heads; whole heads of the 128K decode
+    config.  Each sample stops after
     about `seconds_each` of oracle time.  Rates are over the flops of the rows
     computed (causal: the visible keys only), or the K/V bytes for decode."""
     import numpy as np
