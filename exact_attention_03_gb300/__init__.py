@@ -202,25 +202,40 @@ def forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0, causal: 
 
 
 def decode_noalloc(q, k, v, scale: Optional[float] = None, out=None, lse=None, stream=None):
-    """Single-query attention (q [B,H,1,D]) through fa_fwd_decode_noalloc,
-    which uses the library's fixed device array instead of allocating a
-    workspace (for callers that must not allocate while they run).  The
-    caller must not run two such calls concurrently on the GPU."""
+    """Single-query attention (q [B,H,1,D], k, v [B,H,Lk,D]) through
+    fa_fwd_decode_noalloc, which uses the library's fixed device array instead
+    of allocating a workspace (for callers that must not allocate while they
+    run).  Pass `out` (bf16 [B,H,1,D]) and `lse` (fp32 [B,H,1]) for a call
+    that allocates nothing at all: when omitted, this wrapper creates them
+    with torch.  The caller must not run two such calls concurrently on the
+    GPU."""
     import torch
 
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, L, D]")
     B, H, Lq, D = q.shape
     if Lq != 1:
         raise ValueError("decode_noalloc takes one query row per head")
+    if k.shape != (B, H, k.shape[2], D) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
     for name, t in (("q", q), ("k", k), ("v", v)):
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, H, 1, D), dtype=torch.bfloat16, device=q.device)
+    elif (tuple(out.shape) != (B, H, 1, D) or out.dtype != torch.bfloat16 or out.device != q.device
+          or not out.is_contiguous()):
+        raise ValueError(f"out must be a contiguous bf16 tensor [B, H, 1, D] on {q.device}")
     if lse is None:
         lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    elif (lse.numel() != B * H or lse.dtype != torch.float32 or lse.device != q.device
+          or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous fp32 tensor of B*H elements on {q.device}")
     st = load().fa_fwd_decode_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                       lse.data_ptr(), B, H, Lk, D, float(scale),
                                       _stream_handle(stream))

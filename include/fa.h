@@ -19,6 +19,13 @@
  *
  * Every entry point is a plain C function: pointers, sizes and a status
  * code.  No entry point takes or returns a PyTorch or C++ type.
+ *
+ * Per-device state: on first use on a device the library looks up the device
+ * addresses of its own device arrays (the error word, the array of
+ * fa_fwd_decode_noalloc) and creates its workspace pool, and keeps them until
+ * the process exits.  They belong to the device's primary context, so the
+ * library must not be used on a device after cudaDeviceReset (or any other
+ * reset of that context) in the same process.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -133,7 +140,10 @@ int fa_wait_selftest(int limit_us, void* stream);
  * All calls share the array: calls whose kernels overlap on the GPU (other
  * streams, other host threads) race on it and must be serialised by the
  * caller.  The array keeps the last call's contents; every slot a call reads
- * is written by the same call first, so nothing needs clearing.
+ * is written by the same call first, so nothing needs clearing.  When the
+ * split count fa_fwd would use fits in the array, the results are bit for bit
+ * those of fa_fwd.  The cached address assumes the device's context is never
+ * reset (see "Per-device state" above).
  * Errors: as fa_fwd.
  */
 int fa_fwd_decode_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,

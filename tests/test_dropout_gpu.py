@@ -90,6 +90,39 @@ def test_keep_mask_bit_exact(D, causal, Lq, p):
     _compare(q, k, v, o, lse, p, seed, offset, causal)
 
 
+@pytest.mark.parametrize("D,causal,Lq,Lk", [
+    (64, False, 200, 384),
+    (128, False, 130, 520),
+    (128, True, 384, 384),
+    (64, True, 448, 448),
+])
+def test_keep_mask_bit_exact_past_the_first_key_tile(D, causal, Lq, Lk):
+    # One call per block of D keys, with v = the identity on that block and
+    # zero elsewhere: O[i, c] = w_(i, blk*D + c) z_(i, blk*D + c) 256 / (256 - t),
+    # so every key tile (counter words j div 16 up to Lk / 16) is read bit by bit.
+    B, H = 1, 2
+    p, seed, offset = 0.1, 0xFEDC_BA98_7654_3210, 77
+    g = torch.Generator().manual_seed(8)
+    q = (torch.randn(B, H, Lq, D, generator=g) * 0.3).to(torch.bfloat16).cuda()
+    k = (torch.randn(B, H, Lk, D, generator=g) * 0.3).to(torch.bfloat16).cuda()
+    t = od.drop_threshold(p)
+    z = [od.keep_mask(h, np.arange(Lq), Lk, t, seed, offset) for h in range(H)]
+    visible = np.tril(np.ones((Lq, Lk), dtype=bool)) if causal else np.ones((Lq, Lk), dtype=bool)
+    seen = np.zeros((H, Lq, Lk), dtype=bool)
+    for blk in range((Lk + D - 1) // D):
+        lo, hi = blk * D, min(Lk, (blk + 1) * D)
+        v = torch.zeros(B, H, Lk, D, dtype=torch.bfloat16)
+        v[:, :, lo:hi, :hi - lo] = torch.eye(hi - lo, D, dtype=torch.bfloat16)
+        o, _ = _run(q, k, v.cuda(), p, seed, offset, causal)
+        for h in range(H):
+            nonzero = to_f64(o[0, h].cpu())[:, :hi - lo] != 0
+            vis = visible[:, lo:hi]
+            assert np.array_equal(nonzero[vis], z[h][:, lo:hi][vis]), (blk, h)
+            assert not nonzero[~vis].any()
+            seen[h, :, lo:hi] = True
+    assert seen.all()
+
+
 @pytest.mark.parametrize("B,H,Lq,Lk,D,causal", [
     (1, 2, 300, 300, 128, True),
     (2, 1, 257, 384, 64, False),

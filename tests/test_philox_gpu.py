@@ -1,0 +1,77 @@
+"""The library's device Philox-4x32-10 (csrc/philox.cuh, the routine the
+dropout kernels call) against the CPU oracle, bit for bit.
+
+The oracle's 32-bit Philox is pinned to Triton's independent implementation
+(tests/test_oracle_philox.py); here a test-only probe kernel
+(tests/philox_probe.cu) runs the library's own routine on the same counters
+and keys, plus 2^16 random ones and counters shaped like the dropout
+contract's, and every output word must agree.
+"""
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+from exact_attention_03_gb300 import build as fa_build
+from oracle.philox import philox4x32_10
+from test_oracle_philox import _cases
+
+pytestmark = pytest.mark.gpu
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def probe():
+    os.makedirs(fa_build.BUILD_DIR, exist_ok=True)
+    so = os.path.join(fa_build.BUILD_DIR, "libphilox_probe.so")
+    cmd = [fa_build.nvcc(), *fa_build.ARCH, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC",
+           "-I", fa_build.CSRC, os.path.join(HERE, "philox_probe.cu"), "-o", so]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    lib = ctypes.CDLL(so)
+    lib.philox_probe.restype = ctypes.c_int
+    lib.philox_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    return lib
+
+
+def _run(lib, recs):
+    recs = np.ascontiguousarray(recs, dtype=np.uint32)
+    out = np.zeros((recs.shape[0], 4), dtype=np.uint32)
+    assert lib.philox_probe(recs.ctypes.data, out.ctypes.data, recs.shape[0]) == 0
+    return out
+
+
+def _oracle(recs):
+    out = np.zeros((recs.shape[0], 4), dtype=np.uint32)
+    keys = {}
+    for i, r in enumerate(recs):
+        keys.setdefault((int(r[4]), int(r[5])), []).append(i)
+    for k, idx in keys.items():
+        idx = np.array(idx)
+        w = philox4x32_10([recs[idx, c].astype(np.uint64) for c in range(4)], k)
+        out[idx] = np.stack(w, axis=1)
+    return out
+
+
+def test_device_philox_matches_oracle_on_the_pinned_cases(probe):
+    ctr, key = _cases()
+    recs = np.array([list(c) + list(k) for c, k in zip(ctr, key)], dtype=np.uint64)
+    got = _run(probe, recs)
+    want = np.array([philox4x32_10(c, k) for c, k in zip(ctr, key)], dtype=np.uint32)
+    assert np.array_equal(got, want)
+
+
+def test_device_philox_matches_oracle_on_random_and_contract_counters(probe):
+    rng = np.random.default_rng(5)
+    n = 1 << 16
+    recs = rng.integers(0, 1 << 32, size=(n, 6), dtype=np.uint64)
+    recs[:, 4:] = recs[:8, 4:][np.arange(n) % 8]          # eight keys
+    # the contract's counters: (j div 16 for keys up to 65536, row, head, offset)
+    m = n // 2
+    recs[:m, 0] = rng.integers(0, 4096, size=m)
+    recs[:m, 1] = rng.integers(0, 65536, size=m)
+    recs[:m, 2] = rng.integers(0, 512, size=m)
+    recs[:m, 3] = rng.choice([0, 1, 123456], size=m)
+    assert np.array_equal(_run(probe, recs), _oracle(recs))
