@@ -112,7 +112,7 @@ def test_keep_mask_bit_exact_past_the_first_key_tile(D, causal, Lq, Lk):
     for blk in range((Lk + D - 1) // D):
         lo, hi = blk * D, min(Lk, (blk + 1) * D)
         v = torch.zeros(B, H, Lk, D, dtype=torch.bfloat16)
-        v[:, :, lo:hi, :hi - lo] = torch.eye(hi - lo, D, dtype=torch.bfloat16)
+        v[:, :, lo:hi, :hi - lo] = torch.eye(hi - lo, dtype=torch.bfloat16)
         o, _ = _run(q, k, v.cuda(), p, seed, offset, causal)
         for h in range(H):
             nonzero = to_f64(o[0, h].cpu())[:, :hi - lo] != 0
