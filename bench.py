@@ -54,7 +54,7 @@ def load_peaks():
 
 _CSRC = "exact_attention_03_gb300/csrc/"
 PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_sm103.cu", "sm103_ptx.cuh", "fa_internal.h", "philox.cuh"))
-PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
+PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64x1_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
                                                 "philox.cuh"))
 DECODE_SOURCES = tuple(_CSRC + f for f in ("fa_decode_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 BACKWARD_SOURCES = tuple(_CSRC + f for f in ("fa_backward_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
@@ -265,13 +265,13 @@ def run_ours(args, rank, world):
     }
     prefill_ms = mean_step  # every launch of the step is the prefill kernel
     achieved = step_flops / (prefill_ms * 1e-3) / 1e12
-    result["roofline"] = {"kernel": "fa_prefill_d64_kernel", "bound": "tensor",
+    result["roofline"] = {"kernel": "fa_prefill_d64x1_kernel", "bound": "tensor",
                           "achieved": round(achieved, 3), "peak": peaks["bf16_tflops"],
                           "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                           "peak_source": f"{peak_src} bf16 burst",
                           "per": "one step (one launch at each of the 8 sweep lengths)",
                           "algorithmic_bytes": sum(w.bytes for w in ws),
-                          "traffic": measured_traffic("fa_prefill_d64_kernel/sweep_d64_step",
+                          "traffic": measured_traffic("fa_prefill_d64x1_kernel/sweep_d64_step",
                                                       PREFILL_D64_SOURCES)}
     del bufs, calls, host
 

@@ -40,10 +40,17 @@ int launch_prefill(const void* q, const void* k, const void* v, void* o, float* 
                    const Dropout& dr = Dropout());
 
 // Head dimension 64 (Lq >= 1): separate P buffer, one MMA issuer per query tile,
-// the two query tiles' softmax groups half an iteration apart.
+// the two query tiles' softmax groups half an iteration apart.  Runs the
+// dropout forward itself and hands the plain forward to launch_prefill_d64x1.
 int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                        int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
                        int* err, const Dropout& dr = Dropout());
+
+// Head dimension 64, one query tile per CTA and two CTAs per SM (twice the
+// work units of launch_prefill_d64, each half the size).
+int launch_prefill_d64x1(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
+                         int* err, const Dropout& dr = Dropout());
 
 // Single-query split-K/V path (Lq == 1).  Arguments already validated.
 // `workspace` must hold n_split * B * H * (D + 2) floats.
