@@ -491,7 +491,7 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
   p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;
-  auto kernel = dr.on ? fa_prefill_d64_kernel<true> : fa_prefill_d64_kernel<false>;
+  auto kernel = fa_prefill_d64_kernel<true>;   // dr.on: the plain forward returned above
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return -4;
   kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);

@@ -19,14 +19,15 @@
 // Shared memory: Q (16 KB), a K ring of 3 slots and a V ring of 2 slots
 // (16 KB each): 96 KB + barriers.  A K slot is free once S of its tile has
 // been computed, a V slot once P V has.
-// Warps: 0 = TMA producer for Q and K, 1 = TMEM allocation + MMA issue,
+// Warps: 0 = TMA producer for Q and K (thread 0 issues Q and K(0) right
+// after setting up the barriers), 1 = TMEM allocation + MMA issue,
 // 2 = TMA producer for V, 3 = idle, 4-7 = softmax + epilogue (one query row
 // per thread; TMEM lane quarter = warp % 4).
 #include "fa_internal.h"
-#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
+#include <type_traits>
 
 namespace fa {
 namespace {
@@ -77,10 +78,6 @@ struct Params {
   int group;   // heads per group of the grid order (K/V of a group stay in L2)
   int causal;
   float scale_log2;
-  // dropout on the weights (the DROP instantiation only): bits from
-  // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
-  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
-  float keep_scale;
 };
 
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
@@ -149,7 +146,6 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
                fmax3(pm[9], pm[10], pm[11]), fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
 }
 
-template <bool DROP>
 __global__ void __launch_bounds__(kThreads, 2)
     fa_prefill_d64x1_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
@@ -207,12 +203,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // thread 0 is the K producer: Q and K(0) start loading before the CTA-wide
+    // synchronisation (slot 0 of the K ring is free at the start)
+    mbar_arrive_expect_tx(bar_q, kTileBytes);
+    tma_load_tile(sQ, &tmQ, bar_q, q0, bh);
+    mbar_arrive_expect_tx(bar_kfull(0), kTileBytes);
+    tma_load_tile(sK, &tmK, bar_kfull(0), 0, bh);
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
-  }
+  if (warp == 2 && lane == 0) tma_prefetch_desc(&tmV);
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -230,12 +228,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) {
         const bool is_k = (warp == 0);
         const int stages = is_k ? kKStages : kVStages;
-        if (is_k) {
-          mbar_arrive_expect_tx(bar_q, kTileBytes);
-          tma_load_tile(sQ, &tmQ, bar_q, q0, bh);
-        }
-        int issued = 0;
-        for (int j = 0; j < n; ++j) {
+        // Q and K(0) were issued by this thread before the CTA-wide sync
+        const int j0 = is_k ? 1 : 0;
+        int issued = j0;
+        for (int j = j0; j < n; ++j) {
           const int s = j % stages;
           const int use = j / stages;
           const uint32_t empty = is_k ? bar_kempty(s) : bar_vempty(s);
@@ -312,145 +308,125 @@ __global__ void __launch_bounds__(kThreads, 2)
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
-    // first key tile with masked keys (past Lk, or above the causal diagonal)
+    // first key tile with masked keys (past Lk, or above the causal diagonal);
+    // they are the last tiles of the row, so the hot loop below has no mask code
     const int j_edge = min(p.Lk / 128, p.causal ? q0 / 128 : (1 << 30));
 
-#pragma unroll 2
-    for (int j = 0; j < n && ok; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.err, kSiteSoftmaxS));
-      if (!ok) break;
+    // One key tile: S -> weights P (bf16, TMEM) and the row statistics.  The
+    // exponentials are taken against the running maximum m_run; afterwards
+    // the tile's row sum is checked: every weight is at most that sum, so a
+    // sum up to 2^kRescaleLog2 means the maximum grew by at most the lazy
+    // rescale bound and the weights stand.  Otherwise (rare) the row maximum
+    // is taken, and where it grew by more, O is rescaled and the same code
+    // runs a second pass over the tile.  A row's first tile takes the
+    // maximum before exponentiating.
+    auto tile = [&](int j, auto masked_tag) -> bool {
+      constexpr bool kMasked = decltype(masked_tag)::value;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.err, kSiteSoftmaxS))) return false;
       float s[128];
       tc_fence_after();
       tmem_ld128_2x64_sync(tS, s);
       tc_fence_before();
       mbar_arrive(bar_sfree);  // S(j) is in registers: S may be overwritten
-
-      float alpha = 1.f;
-      bool resc = false;    // warp-uniform: O is multiplied by alpha before PV(j)
-      float2 acc[4];
-      const float2 c2 = make_float2(c, c);
-      float2 nm2 = make_float2(0.f, 0.f);
-      // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
-      auto exp_block = [&](int cb, uint32_t (&w)[16]) {
-        uint4 dw;          // dropout bits of the current 16 keys
-        uint32_t keep4;    // keep bytes of the current 4 keys
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int e = 32 * cb + 2 * i;
-          if constexpr (DROP)
-            if ((i & 7) == 0)
-              dw = philox4x32_10(make_uint4(uint32_t(j * 128 + e) >> 4, uint32_t(qrow), uint32_t(bh), p.offset),
-                                 p.seed_lo, p.seed_hi);
-          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
-          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
-          w[i] = pack_bf16x2(pr.x, pr.y);
-          if constexpr (DROP) {
-            if ((i & 1) == 0) {
-              const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
-                                  : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
-              keep4 = __vcmpgeu4(wsel, p.drop_t4);
-            }
-            w[i] &= dropout_pair_mask(keep4, i & 1);
-          }
-        }
-      };
-      auto rescale_o = [&]() {
-#pragma unroll 1
-        for (int cc = 0; cc < kD; cc += 16) {
-          float ov[16];
-          tmem_ld16_sync(tO + cc, ov);
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(ov[i] * alpha);
-          tmem_st16(tO + cc, w);
-        }
-      };
-      uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P
-      const int k0 = j * 128;
-      if (j >= j_edge) {
+      if constexpr (kMasked) {
+        const int k0 = j * 128;
         const int lim = min(p.Lk - k0, p.causal ? qrow - k0 + 1 : 128);
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i >= lim) s[i] = -INFINITY;
       }
-      // Until a row has a finite running maximum its first tile takes the
-      // maximum before exponentiating; later tiles exponentiate against the
-      // running maximum and check the result afterwards (below).  With dropout
-      // every tile takes the maximum first: a recomputed tile would draw its
-      // random bits twice.
-      const bool exact = DROP || __any_sync(0xffffffffu, m_run == -INFINITY);
-      if (exact) {
-        const float m_cand = fmaxf(m_run, row_max128(s) * c);
-        resc = __any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2);
-        if (resc) {
-          alpha = ex2_approx(m_run - ((m_cand == -INFINITY) ? 0.f : m_cand));
-          m_run = m_cand;
+      float alpha = 1.f;    // O and l are multiplied by alpha (the maximum moved)
+      bool resc = false;    // warp-uniform
+      bool take_max = __any_sync(0xffffffffu, m_run == -INFINITY);
+      bool redo = false;
+      bool waited = (j == 0);   // PV(j-1) has completed: O is stable, P is free
+      float2 acc[4];
+      float2 a03;
+      const float2 c2 = make_float2(c, c);
+      float2 nm2;
+      // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
+      auto exp_block = [&](int cb, uint32_t (&w)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int e = 32 * cb + 2 * i;
+          const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
+          const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          w[i] = pack_bf16x2(pr.x, pr.y);
         }
-      }
-      {
-        const float m_safe = (m_run == -INFINITY) ? 0.f : m_run;
-        nm2 = make_float2(-m_safe, -m_safe);
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
-      exp_block(0, pk[0]);
-      exp_block(1, pk[1]);
-
-      // PV(j-1) has completed: O is stable and P is free
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
-        if (!ok) break;
-      }
-      tc_fence_after();
-      if (resc && j > 0) rescale_o();
-      tmem_st16(tP, pk[0]);
-      tmem_st16(tP + 16, pk[1]);
-      // keys 64-127: computed and stored now that P is free
-#pragma unroll
-      for (int cb = 2; cb < 4; ++cb) {
-        uint32_t w[16];
-        exp_block(cb, w);
-        tmem_st16(tP + 16 * cb, w);
-      }
-      float2 a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-      if (!exact) {
-        // Every weight 2^(c s - m_run) is at most the tile's row sum, so a sum
-        // up to 2^kRescaleLog2 means the maximum grew by at most kRescaleLog2
-        // and the weights stand (the lazy rescale rule).  Otherwise take the
-        // maximum, and where it grew further, rescale and recompute the tile.
-        const bool check = !(a03.x + a03.y <= kRescaleBound);
-        if (__any_sync(0xffffffffu, check)) {
+      };
+      for (;;) {
+        if (take_max) {
           const float m_cand = fmaxf(m_run, row_max128(s) * c);
           if (__any_sync(0xffffffffu, m_cand > m_run + kRescaleLog2)) {
-            alpha = ex2_approx(m_run - m_cand);
+            alpha = ex2_approx(m_run - ((m_cand == -INFINITY) ? 0.f : m_cand));
             m_run = m_cand;
-            nm2 = make_float2(-m_cand, -m_cand);
-#pragma unroll
-            for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int cb = 0; cb < 4; ++cb) {
-              uint32_t w[16];
-              exp_block(cb, w);
-              tmem_st16(tP + 16 * cb, w);
-            }
-            a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
-            if (j > 0) rescale_o();
+            resc = true;
+          } else if (redo) {
+            break;   // the maximum grew by at most the bound: the first pass stands
           }
         }
+        {
+          const float m_safe = (m_run == -INFINITY) ? 0.f : m_run;
+          nm2 = make_float2(-m_safe, -m_safe);
+        }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+        uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P
+        exp_block(0, pk[0]);
+        exp_block(1, pk[1]);
+        if (!waited) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_pv, (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO)))
+            return false;
+          waited = true;
+        }
+        tc_fence_after();
+        if (resc && j > 0) {
+#pragma unroll 1
+          for (int cc = 0; cc < kD; cc += 16) {
+            float ov[16];
+            tmem_ld16_sync(tO + cc, ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(ov[i] * alpha);
+            tmem_st16(tO + cc, w);
+          }
+        }
+        tmem_st16(tP, pk[0]);
+        tmem_st16(tP + 16, pk[1]);
+        // keys 64-127: computed and stored now that P is free
+#pragma unroll
+        for (int cb = 2; cb < 4; ++cb) {
+          uint32_t w[16];
+          exp_block(cb, w);
+          tmem_st16(tP + 16 * cb, w);
+        }
+        a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        if (take_max) break;
+        if (!__any_sync(0xffffffffu, !(a03.x + a03.y <= kRescaleBound))) break;
+        take_max = true;
+        redo = true;
       }
       l_run = l_run * alpha + (a03.x + a03.y);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar_p);
-    }
+      return true;
+    };
+    // (the loop body unrolled by two measured 2-3 % slower, with more stalls
+    // on instruction fetch)
+    const int j_hot = min(n, j_edge);
+#pragma unroll 1
+    for (int j = 0; j < j_hot && ok; ++j) ok = tile(j, std::false_type{});
+#pragma unroll 1
+    for (int j = j_hot; j < n && ok; ++j) ok = tile(j, std::true_type{});
 
     // epilogue: wait for the last PV, then O / l -> bf16, LSE
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_pv, (n - 1) & 1, abort_flag, p.err, kSiteSoftmaxO));
     if (ok) {
       tc_fence_after();
-      const float inv_l = DROP ? p.keep_scale / l_run : 1.f / l_run;
+      const float inv_l = 1.f / l_run;
       const bool valid = qrow < p.Lq;
       __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * kD;
 #pragma unroll 1
@@ -502,14 +478,10 @@ int launch_prefill_d64x1(const void* q, const void* k, const void* v, void* o, f
   p.group = l2_head_group(BH, 2ll * Lk * 64 * 2);   // K and V of a head
   p.causal = causal;
   p.scale_log2 = scale * 1.44269504088896340736f;
-  p.seed_lo = dr.seed_lo;
-  p.seed_hi = dr.seed_hi;
-  p.offset = dr.offset;
-  p.drop_t4 = dr.t * 0x01010101u;
-  p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;
-  auto kernel = dr.on ? fa_prefill_d64x1_kernel<true> : fa_prefill_d64x1_kernel<false>;
+  if (dr.on) return -2;   // the dropout forward runs on fa_prefill_d64_sm103.cu
+  auto kernel = fa_prefill_d64x1_kernel;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return -4;
   kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
