@@ -53,7 +53,7 @@ def load_peaks():
 
 
 _CSRC = "exact_attention_03_gb300/csrc/"
-PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_sm103.cu", "sm103_ptx.cuh", "fa_internal.h", "philox.cuh"))
+PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d128_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64x1_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
                                                 "philox.cuh"))
 DECODE_SOURCES = tuple(_CSRC + f for f in ("fa_decode_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
@@ -311,7 +311,7 @@ def per_config(args, fa, flush, dev, peaks, check):
                           "traffic": None if tr is None else tr * w.B})
         else:
             tf = w.flops / (ms * 1e-3) / 1e12
-            tr = (measured_traffic("fa_prefill_kernel<128>/causal_l8k_d128", PREFILL_SOURCES)
+            tr = (measured_traffic("fa_prefill_d128_kernel/causal_l8k_d128", PREFILL_SOURCES)
                   if name == "causal_l8k_d128" else None)
             entry.update({"TFLOPS": round(tf, 2), "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
                           "frac_bf16_sustained": round(tf / peaks["bf16_tflops_sustained"], 4),

@@ -307,6 +307,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float c = p.scale_log2;
     float m_run = -INFINITY;
     float l_run = 0.f;
+    // after a tile had to be recomputed, the warp's remaining tiles take the
+    // maximum first (sharp logits keep moving the maximum of some row past
+    // the bound, and a recomputed tile costs a second pass of exponentials)
+    bool exact_rest = false;
     bool ok = true;
     // first key tile with masked keys (past Lk, or above the causal diagonal);
     // they are the last tiles of the row, so the hot loop below has no mask code
@@ -318,8 +322,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // sum up to 2^kRescaleLog2 means the maximum grew by at most the lazy
     // rescale bound and the weights stand.  Otherwise (rare) the row maximum
     // is taken, and where it grew by more, O is rescaled and the same code
-    // runs a second pass over the tile.  A row's first tile takes the
-    // maximum before exponentiating.
+    // runs a second pass over the tile.  A row's first tile, and every tile
+    // after a second pass, take the maximum before exponentiating.
     auto tile = [&](int j, auto masked_tag) -> bool {
       constexpr bool kMasked = decltype(masked_tag)::value;
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag, p.err, kSiteSoftmaxS))) return false;
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       float alpha = 1.f;    // O and l are multiplied by alpha (the maximum moved)
       bool resc = false;    // warp-uniform
-      bool take_max = __any_sync(0xffffffffu, m_run == -INFINITY);
+      bool take_max = exact_rest || __any_sync(0xffffffffu, m_run == -INFINITY);
       bool redo = false;
       bool waited = (j == 0);   // PV(j-1) has completed: O is stable, P is free
       float2 acc[4];
@@ -365,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           } else if (redo) {
             break;   // the maximum grew by at most the bound: the first pass stands
           }
+          if (redo) exact_rest = true;
         }
         {
           const float m_safe = (m_run == -INFINITY) ? 0.f : m_run;

@@ -1,5 +1,7 @@
-// fa_prefill_sm103.cu - attention forward for Lq >= 1 on sm_103a (head dimension 128;
-// head dimension 64 dispatches to fa_prefill_d64_sm103.cu).
+// fa_prefill_sm103.cu - attention forward with dropout on the weights, head
+// dimension 128, on sm_103a (launch_prefill also dispatches: the plain
+// forward at D = 128 runs on fa_prefill_d128_sm103.cu, and D = 64 on
+// fa_prefill_d64x1_sm103.cu / fa_prefill_d64_sm103.cu).
 //
 // One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
 // streams that head's K/V in 128-key tiles through a shared-memory ring.
@@ -550,7 +552,7 @@ int launch_prefill(const void* q, const void* k, const void* v, void* o, float* 
   if (D == 64) return launch_prefill_d64(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err, dr);
   if (D == 128)
     return dr.on ? launch<128, true>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, dr, stream, err)
-                 : launch<128, false>(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, dr, stream, err);
+                 : launch_prefill_d128(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err);
   return -2;
 }
 
