@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libfa_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["fa_api.cu", "fa_prefill_sm103.cu", "fa_prefill_d64_sm103.cu",
+SOURCES = ["fa_api.cu", "fa_prefill_d64_sm103.cu",
            "fa_prefill_d64x1_sm103.cu", "fa_prefill_d128_sm103.cu", "fa_decode_sm103.cu",
            "fa_decode_noalloc.cu", "fa_softmax_sm103.cu", "fa_backward_sm103.cu", "fa_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

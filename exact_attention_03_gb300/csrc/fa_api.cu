@@ -122,6 +122,16 @@ int make_tensor_map_bf16(CUtensorMap* map, const void* ptr, int BH, int L, int D
   return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// Prefill / general path: head dimension 64 (fa_prefill_d64x1_sm103.cu, or
+// fa_prefill_d64_sm103.cu with dropout) or 128 (fa_prefill_d128_sm103.cu).
+int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err,
+                   const Dropout& dr) {
+  if (D == 64) return launch_prefill_d64(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err, dr);
+  if (D == 128) return launch_prefill_d128(q, k, v, o, lse, B, H, Lq, Lk, scale, causal, stream, err, dr);
+  return -2;
+}
+
 int num_sms_of_current_device(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;

@@ -46,11 +46,11 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
                        int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
                        int* err, const Dropout& dr = Dropout());
 
-// Head dimension 128 without dropout: the weights P in tensor memory, one
-// S buffer shared by the CTA's two query tiles, one MMA-issuing thread.
+// Head dimension 128: the weights P in tensor memory, one S buffer shared by
+// the CTA's two query tiles, one MMA-issuing thread per query tile.
 int launch_prefill_d128(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
-                        int* err);
+                        int* err, const Dropout& dr = Dropout());
 
 // Head dimension 64, one query tile per CTA and two CTAs per SM (twice the
 // work units of launch_prefill_d64, each half the size).

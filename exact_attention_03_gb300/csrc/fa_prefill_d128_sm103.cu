@@ -1,20 +1,28 @@
 // fa_prefill_d128_sm103.cu - attention forward for head dimension 128 on
-// sm_103a with the weights P kept in tensor memory.
+// sm_103a (plain, and with dropout on the weights).
 //
-// The computation is that of fa_prefill_sm103.cu: two 128-row query tiles
-// (Q0, Q1) of one (batch, head) per CTA, S = Q K^T and O += P V on the
-// tensor cores, and the online-softmax recurrence of "NTU Hung-yi Lee ML 2026
-// Guide: Faster Generation, Part 1: Flash Attention" (quidproquo.cc), "Expand:
-// why multiplying by exp(d1 - d2) fixes it" and "Expand: the correction for
-// the output O", in base 2 with a lazily applied rescale (the running maximum
-// moves only when it grows by more than 2^8; the guide's rescale identity
-// holds for any common reference value).  What differs is where the data
-// lives and in which order the products run:
+// Two 128-row query tiles (Q0, Q1) of one (batch, head) per CTA; S = Q K^T
+// and O += P V on the 5th-generation tensor cores, the weights computed in
+// between on CUDA cores (one query row per thread) with the online-softmax
+// recurrence of "NTU Hung-yi Lee ML 2026 Guide: Faster Generation, Part 1:
+// Flash Attention" (quidproquo.cc), "Expand: why multiplying by exp(d1 - d2)
+// fixes it" and "Expand: the correction for the output O": with d the
+// running max and s the running denominator, a new tile moves d to max(d,
+// tile max), multiplies s and O by exp(d_old - d_new) and adds the tile's
+// terms.  O is kept unnormalised (the guide's O_k multiplied through by s_k)
+// and divided by s once at the end; everything runs in base 2 (x = score *
+// scale * log2 e) and the running maximum moves only when it grows by more
+// than 2^8 (the guide's rescale identity holds for any common reference
+// value, and the bound keeps every weight <= 2^8).  Data placement and the
+// order of the products:
 //
 //  * TMEM (512 columns): S [0,128) shared by the two query tiles, P0
 //    [128,192) and P1 [192,256) (bf16 pairs, 128 keys each), O0 [256,384),
-//    O1 [384,512).  P V reads P from TMEM and only V from shared memory; the
-//    softmax stores P with tcgen05.st instead of shared-memory stores.
+//    O1 [384,512).  P V reads P from TMEM and only V from shared memory, and
+//    the softmax stores P with tcgen05.st (an earlier design kept P in
+//    shared memory, with one S buffer per query tile: 7 % slower on the
+//    causal 8K workload, as both products streamed two operands from shared
+//    memory and every P store waited for the previous P V).
 //  * Each query tile has its own MMA-issuing thread, which issues S_t(j) and
 //    then P_t(j-1) V(j-1).  S_t(j) overwrites the S of the other query tile
 //    once that tile's softmax holds it in registers (S0(0), S1(0), S0(1),
@@ -34,6 +42,7 @@
 // softmax + epilogue of Q1 (one query row per thread; TMEM lane quarter =
 // warp % 4).
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
@@ -92,6 +101,10 @@ struct Params {
   int group;   // heads per group of the grid order (K/V of a group stay in L2)
   int causal;
   float scale_log2;
+  // dropout on the weights (the DROP instantiation only): bits from
+  // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
+  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
+  float keep_scale;
 };
 
 // Bounded wait that ignores the abort flag: used only to drain this CTA's own
@@ -118,6 +131,7 @@ __device__ __forceinline__ float row_max128(const float (&s)[128]) {
                fmax3(pm[9], pm[10], pm[11]), fmax3(fmax3(pm[12], pm[13], pm[14]), pm[15], -INFINITY));
 }
 
+template <bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_prefill_d128_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
@@ -357,7 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float alpha = 1.f;    // O and l are multiplied by alpha (the maximum moved)
       bool resc = false;    // warp-uniform
-      bool take_max = exact_left > 0 || __any_sync(0xffffffffu, m_run == -INFINITY);
+      // with dropout every tile takes the maximum first: a recomputed tile
+      // would draw its random bits twice
+      bool take_max = DROP || exact_left > 0 || __any_sync(0xffffffffu, m_run == -INFINITY);
       if (exact_left > 0) --exact_left;
       bool redo = false;
       bool waited = (j == 0);   // P_t(j-1) V has completed: O_t is stable, P_t is free
@@ -367,13 +383,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 nm2;
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
+        uint4 dw, dw2;     // dropout bits of the block's two groups of 16 keys
+        uint32_t keep4;    // keep bytes of the current 4 keys
+        if constexpr (DROP) {
+          const uint32_t g16 = uint32_t(j * 128 + 32 * cb) >> 4;
+          dw = make_uint4(g16, uint32_t(qrow), uint32_t(bh), p.offset);
+          dw2 = make_uint4(g16 + 1u, uint32_t(qrow), uint32_t(bh), p.offset);
+          philox4x32_10_x2(dw, dw2, p.seed_lo, p.seed_hi);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
+          if constexpr (DROP)
+            if (i == 8) dw = dw2;
           const int e = 32 * cb + 2 * i;
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);
+          acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
           w[i] = pack_bf16x2(pr.x, pr.y);
+          if constexpr (DROP) {
+            if ((i & 1) == 0) {
+              const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
+                                  : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
+              keep4 = __vcmpgeu4(wsel, p.drop_t4);
+            }
+            w[i] &= dropout_pair_mask(keep4, i & 1);
+          }
         }
       };
       for (;;) {
@@ -447,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(bar_o(t), 0, abort_flag, p.err, kSiteSoftmaxO));
     if (ok && n > 0) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = DROP ? p.keep_scale / l_run : 1.f / l_run;
       const bool valid = qrow < p.Lq;
       __nv_bfloat16* orow = p.o + (size_t(bh) * p.Lq + (valid ? qrow : 0)) * kD;
 #pragma unroll 1
@@ -482,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 int launch_prefill_d128(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int Lq, int Lk, float scale, int causal, cudaStream_t stream,
-                        int* err) {
+                        int* err, const Dropout& dr) {
   const int BH = B * H;
   CUtensorMap mq, mk, mv;
   int st = make_tensor_map_bf16(&mq, q, BH, Lq, kD);
@@ -500,12 +534,17 @@ int launch_prefill_d128(const void* q, const void* k, const void* v, void* o, fl
   p.group = l2_head_group(BH, 2ll * Lk * kD * 2);   // K and V of a head
   p.causal = causal;
   p.scale_log2 = scale * 1.44269504088896340736f;
+  p.seed_lo = dr.seed_lo;
+  p.seed_hi = dr.seed_hi;
+  p.offset = dr.offset;
+  p.drop_t4 = dr.t * 0x01010101u;
+  p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;
-  if (cudaFuncSetAttribute(fa_prefill_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
+  auto kernel = dr.on ? fa_prefill_d128_kernel<true> : fa_prefill_d128_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return -4;
-  fa_prefill_d128_kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
+  kernel<<<dim3(unsigned(nblk)), dim3(kThreads), kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 

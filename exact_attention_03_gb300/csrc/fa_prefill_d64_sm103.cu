@@ -2,7 +2,7 @@
 // with dropout on the weights (the plain forward at D = 64 runs on
 // fa_prefill_d64x1_sm103.cu, one query tile per CTA).
 //
-// Same computation as fa_prefill_sm103.cu (two 128-row query tiles per CTA,
+// Two 128-row query tiles per CTA,
 // S = Q K^T and O += P V on the tensor cores, the online-softmax recurrence of
 // "NTU Hung-yi Lee ML 2026 Guide: Faster Generation, Part 1: Flash Attention"
 // (quidproquo.cc), "Expand: why multiplying by exp(d1 - d2) fixes it" and

@@ -31,6 +31,23 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// Two counters under one key, their rounds interleaved so that the two
+// independent multiply chains overlap; the same bits as two philox4x32_10
+// calls.
+__device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
+    const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
+    const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
+    const uint32_t bhi1 = __umulhi(0xCD9E8D57u, b.z), blo1 = 0xCD9E8D57u * b.z;
+    a = make_uint4(ahi1 ^ a.y ^ k0, alo1, ahi0 ^ a.w ^ k1, alo0);
+    b = make_uint4(bhi1 ^ b.y ^ k0, blo1, bhi0 ^ b.w ^ k1, blo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
 // Masks for packed bf16 pairs: `keep4` = __vcmpgeu4(word, t * 0x01010101)
 // holds 0xff in each kept key's byte and 0 in each dropped one; the pair of
 // keys 2m, 2m+1 (m = half) of that word gets 0xffff over each kept element's

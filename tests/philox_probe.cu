@@ -23,11 +23,26 @@ __global__ void philox_probe_kernel(const uint32_t* in, uint32_t* out, int n) {
   o[3] = w.w;
 }
 
+// the paired form: records 2m and 2m+1 share record 2m's key
+__global__ void philox_probe_x2_kernel(const uint32_t* in, uint32_t* out, int npairs) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= npairs) return;
+  const uint32_t* r = in + 12 * size_t(m);
+  uint4 a = make_uint4(r[0], r[1], r[2], r[3]);
+  uint4 b = make_uint4(r[6], r[7], r[8], r[9]);
+  fa::philox4x32_10_x2(a, b, r[4], r[5]);
+  uint32_t* o = out + 8 * size_t(m);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
 }  // namespace
 
-// Host buffers in and out; returns 0 or the CUDA error code.
-extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n) {
+// Host buffers in and out; returns 0 or the CUDA error code.  pairs != 0
+// runs the paired routine (n even; records 2m, 2m+1 under record 2m's key).
+extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int pairs) {
   if (n <= 0 || in_host == nullptr || out_host == nullptr) return -1;
+  if (pairs && (n & 1)) return -1;
   uint32_t* d_in = nullptr;
   uint32_t* d_out = nullptr;
   cudaError_t e = cudaMalloc(&d_in, size_t(n) * 6 * sizeof(uint32_t));
@@ -35,7 +50,10 @@ extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n) 
   if (e == cudaSuccess)
     e = cudaMemcpy(d_in, in_host, size_t(n) * 6 * sizeof(uint32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) {
-    philox_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
+    if (pairs)
+      philox_probe_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
+    else
+      philox_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     e = cudaGetLastError();
   }
   if (e == cudaSuccess)

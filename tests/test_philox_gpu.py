@@ -3,9 +3,10 @@ dropout kernels call) against the CPU oracle, bit for bit.
 
 The oracle's 32-bit Philox is pinned to Triton's independent implementation
 (tests/test_oracle_philox.py); here a test-only probe kernel
-(tests/philox_probe.cu) runs the library's own routine on the same counters
-and keys, plus 2^16 random ones and counters shaped like the dropout
-contract's, and every output word must agree.
+(tests/philox_probe.cu) runs the library's own routines (one counter, and two
+counters under one key with their rounds interleaved) on the same counters
+and keys, plus random ones and counters shaped like the dropout contract's,
+and every output word must agree.
 """
 import ctypes
 import os
@@ -32,14 +33,14 @@ def probe():
     assert r.returncode == 0, r.stderr
     lib = ctypes.CDLL(so)
     lib.philox_probe.restype = ctypes.c_int
-    lib.philox_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    lib.philox_probe.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int]
     return lib
 
 
-def _run(lib, recs):
+def _run(lib, recs, pairs=0):
     recs = np.ascontiguousarray(recs, dtype=np.uint32)
     out = np.zeros((recs.shape[0], 4), dtype=np.uint32)
-    assert lib.philox_probe(recs.ctypes.data, out.ctypes.data, recs.shape[0]) == 0
+    assert lib.philox_probe(recs.ctypes.data, out.ctypes.data, recs.shape[0], pairs) == 0
     return out
 
 
@@ -75,3 +76,16 @@ def test_device_philox_matches_oracle_on_random_and_contract_counters(probe):
     recs[:m, 2] = rng.integers(0, 512, size=m)
     recs[:m, 3] = rng.choice([0, 1, 123456], size=m)
     assert np.array_equal(_run(probe, recs), _oracle(recs))
+
+
+def test_paired_device_philox_matches_oracle(probe):
+    # the two-counter routine the D = 128 dropout kernels use: records 2m and
+    # 2m+1 share a key, as the two 16-key groups of a 32-key block do
+    rng = np.random.default_rng(6)
+    n = 1 << 14
+    recs = rng.integers(0, 1 << 32, size=(n, 6), dtype=np.uint64)
+    recs[1::2, 4:] = recs[0::2, 4:]
+    recs[0::2, 0] = rng.integers(0, 4096, size=n // 2)
+    recs[1::2, 0] = recs[0::2, 0] + 1
+    recs[1::2, 1:4] = recs[0::2, 1:4]
+    assert np.array_equal(_run(probe, recs, pairs=1), _oracle(recs))
