@@ -54,8 +54,7 @@ def load_peaks():
 
 _CSRC = "exact_attention_03_gb300/csrc/"
 PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d128_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
-PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64x1_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
-                                                "philox.cuh"))
+PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64x1_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 DECODE_SOURCES = tuple(_CSRC + f for f in ("fa_decode_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 BACKWARD_SOURCES = tuple(_CSRC + f for f in ("fa_backward_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 
