@@ -337,6 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + kColO + t * kD;
     const float c = p.scale_log2;
     const int n = t ? nt1 : nt0;
+    // the parts of the Philox rounds shared by all of this row's calls
+    PhiloxRow prow;
+    if constexpr (DROP) prow = philox_row(uint32_t(qrow), uint32_t(bh), p.offset, p.seed_lo, p.seed_hi);
     float m_run = -INFINITY;
     float l_run = 0.f;
     int exact_left = 0;   // tiles that take the maximum first (warp-uniform)
@@ -387,9 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t keep4;    // keep bytes of the current 4 keys
         if constexpr (DROP) {
           const uint32_t g16 = uint32_t(j * 128 + 32 * cb) >> 4;
-          dw = make_uint4(g16, uint32_t(qrow), uint32_t(bh), p.offset);
-          dw2 = make_uint4(g16 + 1u, uint32_t(qrow), uint32_t(bh), p.offset);
-          philox4x32_10_x2(dw, dw2, p.seed_lo, p.seed_hi);
+          philox4x32_10_row_x2(g16, g16 + 1u, prow, dw, dw2);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {

@@ -279,6 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + kColO + t * kD;
     const float c = p.scale_log2;
     const int n = t ? nt1 : nt0;
+    // the parts of the Philox rounds shared by all of this row's calls
+    PhiloxRow prow;
+    if constexpr (DROP) prow = philox_row(uint32_t(qrow), uint32_t(bh), p.offset, p.seed_lo, p.seed_hi);
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
@@ -313,8 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = 32 * cb + 2 * i;
           if constexpr (DROP)
             if ((i & 7) == 0)
-              dw = philox4x32_10(make_uint4(uint32_t(j * 128 + e) >> 4, uint32_t(qrow), uint32_t(bh), p.offset),
-                                 p.seed_lo, p.seed_hi);
+              dw = philox4x32_10_row(uint32_t(j * 128 + e) >> 4, prow);
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights

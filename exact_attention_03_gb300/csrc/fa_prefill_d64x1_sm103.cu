@@ -377,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 #pragma unroll
         for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
-        uint32_t pk[2][16];   // P of keys 0-63, computed before PV(j-1) has freed P
-        exp_block(0, pk[0]);
-        exp_block(1, pk[1]);
+        uint32_t pk[32];   // P of keys 0-63, computed before PV(j-1) has freed P
+        exp_block(0, *reinterpret_cast<uint32_t(*)[16]>(pk));
+        exp_block(1, *reinterpret_cast<uint32_t(*)[16]>(pk + 16));
         if (!waited) {
           if (!__all_sync(0xffffffffu, mbar_wait(bar_pv, (j - 1) & 1, abort_flag, p.err, kSiteSoftmaxO)))
             return false;
@@ -397,14 +397,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             tmem_st16(tO + cc, w);
           }
         }
-        tmem_st16(tP, pk[0]);
-        tmem_st16(tP + 16, pk[1]);
+        // each half of P in one 32-column store (fewer TMEM accesses beside the products)
+        tmem_st32(tP, pk);
         // keys 64-127: computed and stored now that P is free
-#pragma unroll
-        for (int cb = 2; cb < 4; ++cb) {
-          uint32_t w[16];
-          exp_block(cb, w);
-          tmem_st16(tP + 16 * cb, w);
+        {
+          uint32_t w[32];
+          exp_block(2, *reinterpret_cast<uint32_t(*)[16]>(w));
+          exp_block(3, *reinterpret_cast<uint32_t(*)[16]>(w + 16));
+          tmem_st32(tP + 32, w);
         }
         a03 = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
         if (take_max) break;

@@ -48,6 +48,75 @@ __device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, uint32_t k0
   }
 }
 
+// The dropout counter (j div 16, i, bh, offset) changes only in word 0 between
+// the calls of one query row, so part of the first two rounds is the same for
+// every call of the row: round 1 multiplies word 2 (bh), round 2 multiplies
+// the word that round 1 made of (bh, i, key).  PhiloxRow holds those values
+// (and the key) once per row; philox4x32_10_row(x, R) then returns exactly
+// philox4x32_10((x, i, bh, offset), k0, k1) with two of the first four
+// products and four key additions per round fewer.
+struct PhiloxRow {
+  uint32_t w0;    // word 0 after round 1: hi(M1 * bh) ^ i ^ k0
+  uint32_t w1k;   // word 1 after round 1, xored with round 2's key 0: (M1 * bh) ^ (k0 + W0)
+  uint32_t w3k;   // offset ^ k1: xored into word 2 by round 1
+  uint32_t h2k;   // hi(M0 * w0) ^ (k1 + W1): round 2's word 2 before the low product of word 0
+  uint32_t l2;    // lo(M0 * w0): round 2's word 3
+  uint32_t k0, k1;
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t i, uint32_t bh, uint32_t offset, uint32_t k0,
+                                                uint32_t k1) {
+  PhiloxRow R;
+  R.w0 = __umulhi(0xCD9E8D57u, bh) ^ i ^ k0;
+  R.w1k = (0xCD9E8D57u * bh) ^ (k0 + 0x9E3779B9u);
+  R.w3k = offset ^ k1;
+  R.h2k = __umulhi(0xD2511F53u, R.w0) ^ (k1 + 0xBB67AE85u);
+  R.l2 = 0xD2511F53u * R.w0;
+  R.k0 = k0;
+  R.k1 = k1;
+  return R;
+}
+
+// rounds 3..10 (r = 2..9) of philox4x32_10 on the state after round 2
+__device__ __forceinline__ uint4 philox_rounds_from_3(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 2; r < 10; ++r) {
+    const uint32_t kr0 = k0 + uint32_t(r) * 0x9E3779B9u, kr1 = k1 + uint32_t(r) * 0xBB67AE85u;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ kr0, lo1, hi0 ^ c.w ^ kr1, lo0);
+  }
+  return c;
+}
+
+// the state after rounds 1 and 2 for counter word 0 = x
+__device__ __forceinline__ uint4 philox_rounds_1_2(uint32_t x, const PhiloxRow& R) {
+  const uint32_t z = __umulhi(0xD2511F53u, x) ^ R.w3k;   // round 1: word 2
+  const uint32_t lo = 0xD2511F53u * x;                     // round 1: word 3
+  return make_uint4(__umulhi(0xCD9E8D57u, z) ^ R.w1k, 0xCD9E8D57u * z, R.h2k ^ lo, R.l2);
+}
+
+__device__ __forceinline__ uint4 philox4x32_10_row(uint32_t x, const PhiloxRow& R) {
+  return philox_rounds_from_3(philox_rounds_1_2(x, R), R.k0, R.k1);
+}
+
+// two counters of one row (word 0 = xa, xb), their rounds interleaved
+__device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, const PhiloxRow& R, uint4& a,
+                                                     uint4& b) {
+  a = philox_rounds_1_2(xa, R);
+  b = philox_rounds_1_2(xb, R);
+#pragma unroll
+  for (int r = 2; r < 10; ++r) {
+    const uint32_t kr0 = R.k0 + uint32_t(r) * 0x9E3779B9u, kr1 = R.k1 + uint32_t(r) * 0xBB67AE85u;
+    const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
+    const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
+    const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
+    const uint32_t bhi1 = __umulhi(0xCD9E8D57u, b.z), blo1 = 0xCD9E8D57u * b.z;
+    a = make_uint4(ahi1 ^ a.y ^ kr0, alo1, ahi0 ^ a.w ^ kr1, alo0);
+    b = make_uint4(bhi1 ^ b.y ^ kr0, blo1, bhi0 ^ b.w ^ kr1, blo0);
+  }
+}
+
 // Masks for packed bf16 pairs: `keep4` = __vcmpgeu4(word, t * 0x01010101)
 // holds 0xff in each kept key's byte and 0 in each dropped one; the pair of
 // keys 2m, 2m+1 (m = half) of that word gets 0xffff over each kept element's

@@ -36,12 +36,39 @@ __global__ void philox_probe_x2_kernel(const uint32_t* in, uint32_t* out, int np
   o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
+// the row routines: record i's counter (x, i, bh, offset) through philox_row
+__global__ void philox_probe_row_kernel(const uint32_t* in, uint32_t* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t* r = in + 6 * size_t(i);
+  const fa::PhiloxRow R = fa::philox_row(r[1], r[2], r[3], r[4], r[5]);
+  const uint4 w = fa::philox4x32_10_row(r[0], R);
+  uint32_t* o = out + 4 * size_t(i);
+  o[0] = w.x; o[1] = w.y; o[2] = w.z; o[3] = w.w;
+}
+
+// records 2m and 2m+1 share words 1-3 and the key of record 2m
+__global__ void philox_probe_row_x2_kernel(const uint32_t* in, uint32_t* out, int npairs) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= npairs) return;
+  const uint32_t* r = in + 12 * size_t(m);
+  const fa::PhiloxRow R = fa::philox_row(r[1], r[2], r[3], r[4], r[5]);
+  uint4 a, b;
+  fa::philox4x32_10_row_x2(r[0], r[6], R, a, b);
+  uint32_t* o = out + 8 * size_t(m);
+  o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
+  o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
 }  // namespace
 
-// Host buffers in and out; returns 0 or the CUDA error code.  pairs != 0
-// runs the paired routine (n even; records 2m, 2m+1 under record 2m's key).
-extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int pairs) {
-  if (n <= 0 || in_host == nullptr || out_host == nullptr) return -1;
+// Host buffers in and out; returns 0 or the CUDA error code.  mode: 0 = the
+// single routine, 1 = the paired routine (n even; records 2m, 2m+1 under
+// record 2m's key), 2 = the row routine, 3 = the paired row routine (records
+// 2m, 2m+1 share words 1-3 and the key).
+extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int mode) {
+  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 3) return -1;
+  const bool pairs = (mode == 1 || mode == 3);
   if (pairs && (n & 1)) return -1;
   uint32_t* d_in = nullptr;
   uint32_t* d_out = nullptr;
@@ -50,8 +77,12 @@ extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, 
   if (e == cudaSuccess)
     e = cudaMemcpy(d_in, in_host, size_t(n) * 6 * sizeof(uint32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) {
-    if (pairs)
+    if (mode == 1)
       philox_probe_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
+    else if (mode == 3)
+      philox_probe_row_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
+    else if (mode == 2)
+      philox_probe_row_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else
       philox_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     e = cudaGetLastError();

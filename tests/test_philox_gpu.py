@@ -3,10 +3,11 @@ dropout kernels call) against the CPU oracle, bit for bit.
 
 The oracle's 32-bit Philox is pinned to Triton's independent implementation
 (tests/test_oracle_philox.py); here a test-only probe kernel
-(tests/philox_probe.cu) runs the library's own routines (one counter, and two
-counters under one key with their rounds interleaved) on the same counters
-and keys, plus random ones and counters shaped like the dropout contract's,
-and every output word must agree.
+(tests/philox_probe.cu) runs the library's own routines (one counter; two
+counters under one key with their rounds interleaved; and the row forms that
+fold the parts of the first two rounds shared by one query row's calls) on
+the same counters and keys, plus random ones and counters shaped like the
+dropout contract's, and every output word must agree.
 """
 import ctypes
 import os
@@ -37,10 +38,10 @@ def probe():
     return lib
 
 
-def _run(lib, recs, pairs=0):
+def _run(lib, recs, mode=0):
     recs = np.ascontiguousarray(recs, dtype=np.uint32)
     out = np.zeros((recs.shape[0], 4), dtype=np.uint32)
-    assert lib.philox_probe(recs.ctypes.data, out.ctypes.data, recs.shape[0], pairs) == 0
+    assert lib.philox_probe(recs.ctypes.data, out.ctypes.data, recs.shape[0], mode) == 0
     return out
 
 
@@ -88,4 +89,17 @@ def test_paired_device_philox_matches_oracle(probe):
     recs[0::2, 0] = rng.integers(0, 4096, size=n // 2)
     recs[1::2, 0] = recs[0::2, 0] + 1
     recs[1::2, 1:4] = recs[0::2, 1:4]
-    assert np.array_equal(_run(probe, recs, pairs=1), _oracle(recs))
+    assert np.array_equal(_run(probe, recs, mode=1), _oracle(recs))
+
+
+@pytest.mark.parametrize("paired", [False, True])
+def test_row_device_philox_matches_oracle(probe, paired):
+    # the row routines the dropout kernels use: words 1-3 (query row, head,
+    # offset) and the key are fixed per row, the key block j div 16 varies
+    rng = np.random.default_rng(7 + paired)
+    n = 1 << 14
+    recs = rng.integers(0, 1 << 32, size=(n, 6), dtype=np.uint64)
+    recs[:n // 2, 0] = rng.integers(0, 4096, size=n // 2)
+    if paired:
+        recs[1::2, 1:] = recs[0::2, 1:]
+    assert np.array_equal(_run(probe, recs, mode=3 if paired else 2), _oracle(recs))
