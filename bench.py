@@ -99,46 +99,76 @@ def sweep_workloads():
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples of the SM clock and the throttle reasons, every 10 ms,
+    started before the timed region; `stop(t0, t1)` keeps the samples whose
+    timestamps fall in the timed region's wall-clock window (+-20 ms; the
+    nearest sample if none does)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
+        import threading
         self.proc = None
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "--format=csv,noheader,nounits", "-lms", "10"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except Exception:
             self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+        # let the sampler start producing before the timed region begins
+        t_end = time.time() + 5.0
+        while not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.01)
 
-    def stop(self):
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+
+    @staticmethod
+    def _epoch(stamp: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp.strip(), fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    def stop(self, t0: float, t1: float):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
+        self.reader.join(timeout=5)
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in out.strip().splitlines():
+        rows = []
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                rows.append((self._epoch(parts[0]), float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        rows = [r for r in rows if r[0] is not None]
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+        if not inside and rows:
+            mid = 0.5 * (t0 + t1)
+            inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "samples": len(inside), "samples_total": len(rows),
+                "window_ms": round((t1 - t0) * 1e3, 1), "reasons": reasons}
 
 
 # ---------------------------------------------------------------- our arm
@@ -191,14 +221,15 @@ def run_ours(args, rank, world):
               fa.forward(q, k, v, causal=w.causal, out=o, lse=lse)) for (w, q, k, v, o, lse) in bufs]
     _time_launches(calls, flush, args.warmup)
     check()
+    clocks = ClockSampler(dev.index)   # started (and producing) before the barrier
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(dev.index)
     t0 = time.perf_counter()
+    w0 = time.time()
     times = _time_launches(calls, flush, args.steps)
     wall = time.perf_counter() - t0
-    clk = clocks.stop()
+    clk = clocks.stop(w0, time.time())
     torch.cuda.synchronize()
     check()
     n = len(calls)
