@@ -103,7 +103,9 @@ struct Params {
   float scale_log2;
   // dropout on the weights (the DROP instantiation only): bits from
   // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
-  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
+  uint32_t seed_lo, seed_hi, offset;
+  uint32_t drop_tl4, drop_hsel;   // (t mod 128) * 0x01010101; all ones iff t >= 128
+  PhiloxKeys keys;                 // round keys 3..10 of the seed
   float keep_scale;
 };
 
@@ -387,10 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
         uint4 dw, dw2;     // dropout bits of the block's two groups of 16 keys
-        uint32_t keep4;    // keep bytes of the current 4 keys
+        uint32_t keep4;    // keep bits (byte top bits) of the current 4 keys
         if constexpr (DROP) {
           const uint32_t g16 = uint32_t(j * 128 + 32 * cb) >> 4;
-          philox4x32_10_row_x2(g16, g16 + 1u, prow, dw, dw2);
+          philox4x32_10_row_x2(g16, g16 + 1u, prow, p.keys, dw, dw2);
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((i & 1) == 0) {
               const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
                                   : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
-              keep4 = __vcmpgeu4(wsel, p.drop_t4);
+              keep4 = dropout_keep_msb(wsel, p.drop_tl4, p.drop_hsel);
             }
             w[i] &= dropout_pair_mask(keep4, i & 1);
           }
@@ -538,7 +540,9 @@ int launch_prefill_d128(const void* q, const void* k, const void* v, void* o, fl
   p.seed_lo = dr.seed_lo;
   p.seed_hi = dr.seed_hi;
   p.offset = dr.offset;
-  p.drop_t4 = dr.t * 0x01010101u;
+  p.drop_tl4 = (dr.t & 0x7fu) * 0x01010101u;
+  p.drop_hsel = dr.t >= 128u ? 0xffffffffu : 0u;
+  p.keys = philox_round_keys(dr.seed_lo, dr.seed_hi);
   p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;

@@ -80,7 +80,9 @@ struct Params {
   float scale_log2;
   // dropout on the weights (the DROP instantiation only): bits from
   // philox.cuh's contract, key kept iff its byte >= t, O scaled by keep_scale
-  uint32_t seed_lo, seed_hi, offset, drop_t4;   // drop_t4 = t * 0x01010101
+  uint32_t seed_lo, seed_hi, offset;
+  uint32_t drop_tl4, drop_hsel;   // (t mod 128) * 0x01010101; all ones iff t >= 128
+  PhiloxKeys keys;                 // round keys 3..10 of the seed
   float keep_scale;
 };
 
@@ -310,13 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
         uint4 dw;          // dropout bits of the current 16 keys
-        uint32_t keep4;    // keep bytes of the current 4 keys
+        uint32_t keep4;    // keep bits (byte top bits) of the current 4 keys
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int e = 32 * cb + 2 * i;
           if constexpr (DROP)
             if ((i & 7) == 0)
-              dw = philox4x32_10_row(uint32_t(j * 128 + e) >> 4, prow);
+              dw = philox4x32_10_row(uint32_t(j * 128 + e) >> 4, prow, p.keys);
           const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), c2, nm2);
           const float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           acc[i & 3] = __fadd2_rn(acc[i & 3], pr);   // the row sum keeps the undropped weights
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((i & 1) == 0) {
               const uint32_t wsel = ((i >> 1) & 3) == 0 ? dw.x : ((i >> 1) & 3) == 1 ? dw.y
                                   : ((i >> 1) & 3) == 2 ? dw.z : dw.w;
-              keep4 = __vcmpgeu4(wsel, p.drop_t4);
+              keep4 = dropout_keep_msb(wsel, p.drop_tl4, p.drop_hsel);
             }
             w[i] &= dropout_pair_mask(keep4, i & 1);
           }
@@ -489,7 +491,9 @@ int launch_prefill_d64(const void* q, const void* k, const void* v, void* o, flo
   p.seed_lo = dr.seed_lo;
   p.seed_hi = dr.seed_hi;
   p.offset = dr.offset;
-  p.drop_t4 = dr.t * 0x01010101u;
+  p.drop_tl4 = (dr.t & 0x7fu) * 0x01010101u;
+  p.drop_hsel = dr.t >= 128u ? 0xffffffffu : 0u;
+  p.keys = philox_round_keys(dr.seed_lo, dr.seed_hi);
   p.keep_scale = dr.keep_scale;
   const long long nblk = (long long)p.n_qblk * BH;
   if (nblk > 0x7fffffffLL) return -2;

@@ -77,14 +77,28 @@ __device__ __forceinline__ PhiloxRow philox_row(uint32_t i, uint32_t bh, uint32_
   return R;
 }
 
+// The round keys of rounds 3..10 (k0 + r W0, k1 + r W1 for r = 2..9): fixed
+// by the seed, so a launch computes them once (host side) and the kernels
+// read them from their parameters instead of bumping the key in every call.
+struct PhiloxKeys {
+  uint32_t k0[8], k1[8];
+};
+__host__ __device__ inline PhiloxKeys philox_round_keys(uint32_t k0, uint32_t k1) {
+  PhiloxKeys K;
+  for (int r = 2; r < 10; ++r) {
+    K.k0[r - 2] = k0 + uint32_t(r) * 0x9E3779B9u;
+    K.k1[r - 2] = k1 + uint32_t(r) * 0xBB67AE85u;
+  }
+  return K;
+}
+
 // rounds 3..10 (r = 2..9) of philox4x32_10 on the state after round 2
-__device__ __forceinline__ uint4 philox_rounds_from_3(uint4 c, uint32_t k0, uint32_t k1) {
+__device__ __forceinline__ uint4 philox_rounds_from_3(uint4 c, const PhiloxKeys& K) {
 #pragma unroll
   for (int r = 2; r < 10; ++r) {
-    const uint32_t kr0 = k0 + uint32_t(r) * 0x9E3779B9u, kr1 = k1 + uint32_t(r) * 0xBB67AE85u;
     const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
     const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-    c = make_uint4(hi1 ^ c.y ^ kr0, lo1, hi0 ^ c.w ^ kr1, lo0);
+    c = make_uint4(hi1 ^ c.y ^ K.k0[r - 2], lo1, hi0 ^ c.w ^ K.k1[r - 2], lo0);
   }
   return c;
 }
@@ -96,18 +110,18 @@ __device__ __forceinline__ uint4 philox_rounds_1_2(uint32_t x, const PhiloxRow& 
   return make_uint4(__umulhi(0xCD9E8D57u, z) ^ R.w1k, 0xCD9E8D57u * z, R.h2k ^ lo, R.l2);
 }
 
-__device__ __forceinline__ uint4 philox4x32_10_row(uint32_t x, const PhiloxRow& R) {
-  return philox_rounds_from_3(philox_rounds_1_2(x, R), R.k0, R.k1);
+__device__ __forceinline__ uint4 philox4x32_10_row(uint32_t x, const PhiloxRow& R, const PhiloxKeys& K) {
+  return philox_rounds_from_3(philox_rounds_1_2(x, R), K);
 }
 
 // two counters of one row (word 0 = xa, xb), their rounds interleaved
-__device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, const PhiloxRow& R, uint4& a,
-                                                     uint4& b) {
+__device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, const PhiloxRow& R,
+                                                     const PhiloxKeys& K, uint4& a, uint4& b) {
   a = philox_rounds_1_2(xa, R);
   b = philox_rounds_1_2(xb, R);
 #pragma unroll
   for (int r = 2; r < 10; ++r) {
-    const uint32_t kr0 = R.k0 + uint32_t(r) * 0x9E3779B9u, kr1 = R.k1 + uint32_t(r) * 0xBB67AE85u;
+    const uint32_t kr0 = K.k0[r - 2], kr1 = K.k1[r - 2];
     const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
     const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
     const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
@@ -117,12 +131,26 @@ __device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, c
   }
 }
 
-// Masks for packed bf16 pairs: `keep4` = __vcmpgeu4(word, t * 0x01010101)
-// holds 0xff in each kept key's byte and 0 in each dropped one; the pair of
-// keys 2m, 2m+1 (m = half) of that word gets 0xffff over each kept element's
-// 16 bits and 0 over a dropped one.
-__device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t keep4, int half) {
-  return __byte_perm(keep4, 0u, half ? 0x3322u : 0x1100u);
+// The keep decision of four keys at once: byte b of `word` is kept iff
+// b >= t.  With b = 128 h + l and t = 128 ht + lt (h, ht the top bits),
+// z = (word | 0x80808080) - lt * 0x01010101 has in each byte 128 + l - lt,
+// between 1 and 255 (no borrow between bytes), whose top bit is l >= lt; so
+// b >= t is the top bit of (b | z) when ht = 0 and of (b & z) when ht = 1.
+// Returns the word whose byte top bits are the keep bits; tl4 = lt *
+// 0x01010101, hsel = all ones when t >= 128, else 0.
+__host__ __device__ inline uint32_t dropout_keep_msb(uint32_t word, uint32_t tl4, uint32_t hsel) {
+  const uint32_t z = (word | 0x80808080u) - tl4;
+  return ((word & z) & hsel) | ((word | z) & ~hsel);
+}
+
+// Mask of a packed bf16 pair from dropout_keep_msb's word: the pair of keys
+// 2m, 2m+1 (m = half) of the word gets 0xffff over each kept element's 16
+// bits and 0 over a dropped one (each selected byte's top bit replicated over
+// two result bytes).
+__device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t keep_msb, int half) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(keep_msb), "r"(half ? 0xBBAAu : 0x9988u));
+  return m;
 }
 
 }  // namespace fa

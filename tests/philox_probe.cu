@@ -42,7 +42,7 @@ __global__ void philox_probe_row_kernel(const uint32_t* in, uint32_t* out, int n
   if (i >= n) return;
   const uint32_t* r = in + 6 * size_t(i);
   const fa::PhiloxRow R = fa::philox_row(r[1], r[2], r[3], r[4], r[5]);
-  const uint4 w = fa::philox4x32_10_row(r[0], R);
+  const uint4 w = fa::philox4x32_10_row(r[0], R, fa::philox_round_keys(r[4], r[5]));
   uint32_t* o = out + 4 * size_t(i);
   o[0] = w.x; o[1] = w.y; o[2] = w.z; o[3] = w.w;
 }
@@ -54,10 +54,25 @@ __global__ void philox_probe_row_x2_kernel(const uint32_t* in, uint32_t* out, in
   const uint32_t* r = in + 12 * size_t(m);
   const fa::PhiloxRow R = fa::philox_row(r[1], r[2], r[3], r[4], r[5]);
   uint4 a, b;
-  fa::philox4x32_10_row_x2(r[0], r[6], R, a, b);
+  fa::philox4x32_10_row_x2(r[0], r[6], R, fa::philox_round_keys(r[4], r[5]), a, b);
   uint32_t* o = out + 8 * size_t(m);
   o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
   o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+
+// the keep masks of the dropout kernels: record i = (word, t, -, -, -, -);
+// out = (mask of keys 0-1, mask of keys 2-3, -, -)
+__global__ void keep_mask_probe_kernel(const uint32_t* in, uint32_t* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t* r = in + 6 * size_t(i);
+  const uint32_t t = r[1];
+  const uint32_t keep = fa::dropout_keep_msb(r[0], (t & 0x7fu) * 0x01010101u, t >= 128u ? 0xffffffffu : 0u);
+  uint32_t* o = out + 4 * size_t(i);
+  o[0] = fa::dropout_pair_mask(keep, 0);
+  o[1] = fa::dropout_pair_mask(keep, 1);
+  o[2] = 0;
+  o[3] = 0;
 }
 
 }  // namespace
@@ -65,9 +80,9 @@ __global__ void philox_probe_row_x2_kernel(const uint32_t* in, uint32_t* out, in
 // Host buffers in and out; returns 0 or the CUDA error code.  mode: 0 = the
 // single routine, 1 = the paired routine (n even; records 2m, 2m+1 under
 // record 2m's key), 2 = the row routine, 3 = the paired row routine (records
-// 2m, 2m+1 share words 1-3 and the key).
+// 2m, 2m+1 share words 1-3 and the key), 4 = the dropout keep masks.
 extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int mode) {
-  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 3) return -1;
+  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 4) return -1;
   const bool pairs = (mode == 1 || mode == 3);
   if (pairs && (n & 1)) return -1;
   uint32_t* d_in = nullptr;
@@ -83,6 +98,8 @@ extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, 
       philox_probe_row_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
     else if (mode == 2)
       philox_probe_row_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
+    else if (mode == 4)
+      keep_mask_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else
       philox_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     e = cudaGetLastError();

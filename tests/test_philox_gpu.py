@@ -5,9 +5,12 @@ The oracle's 32-bit Philox is pinned to Triton's independent implementation
 (tests/test_oracle_philox.py); here a test-only probe kernel
 (tests/philox_probe.cu) runs the library's own routines (one counter; two
 counters under one key with their rounds interleaved; and the row forms that
-fold the parts of the first two rounds shared by one query row's calls) on
-the same counters and keys, plus random ones and counters shaped like the
-dropout contract's, and every output word must agree.
+fold the parts of the first two rounds shared by one query row's calls and
+take the later rounds' keys precomputed) on the same counters and keys, plus
+random ones and counters shaped like the dropout contract's, and every output
+word must agree.  The same probe runs the kernels' keep masks (four random
+bytes against the threshold t at once) for every t and every byte value,
+against the plain comparison byte >= t.
 """
 import ctypes
 import os
@@ -103,3 +106,21 @@ def test_row_device_philox_matches_oracle(probe, paired):
     if paired:
         recs[1::2, 1:] = recs[0::2, 1:]
     assert np.array_equal(_run(probe, recs, mode=3 if paired else 2), _oracle(recs))
+
+
+def test_keep_masks_match_the_byte_comparison_for_every_threshold(probe):
+    # every byte value in every position, for every threshold t = 0..255
+    vals = np.arange(256, dtype=np.uint64)
+    words = np.concatenate([vals * 0x01010101,                       # all four bytes equal
+                            vals | ((255 - vals) << 8) | (((vals * 7) % 256) << 16) | (((vals * 13 + 5) % 256) << 24)])
+    recs = np.zeros((256 * len(words), 6), dtype=np.uint64)
+    recs[:, 0] = np.tile(words, 256)
+    recs[:, 1] = np.repeat(np.arange(256, dtype=np.uint64), len(words))
+    got = _run(probe, recs, mode=4)
+    w = recs[:, 0].astype(np.uint32)
+    t = recs[:, 1].astype(np.uint32)
+    keep = [((w >> (8 * b)) & 0xff) >= t for b in range(4)]
+    half = lambda k: np.where(k, np.uint32(0xffff), np.uint32(0))
+    want_lo = half(keep[0]) | (half(keep[1]) << np.uint32(16))
+    want_hi = half(keep[2]) | (half(keep[3]) << np.uint32(16))
+    assert np.array_equal(got[:, 0], want_lo) and np.array_equal(got[:, 1], want_hi)
