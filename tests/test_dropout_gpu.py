@@ -65,7 +65,7 @@ def _compare(q, k, v, o, lse, p, seed, offset, causal):
 
 
 @pytest.mark.parametrize("D,causal,Lq", [(64, False, 300), (64, True, 64), (128, False, 200), (128, True, 128)])
-@pytest.mark.parametrize("p", [0.1, 0.5])
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.8])
 def test_keep_mask_bit_exact(D, causal, Lq, p):
     # v = identity over the Lk = D keys: O[i, j] = w_ij z_ij 256 / (256 - t)
     B, H, Lk = 1, 2, D
