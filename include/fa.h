@@ -1,5 +1,7 @@
 /*
- * fa.h - C ABI of the GB300 (sm_103a) exact-attention forward library.
+ * fa.h - C ABI of the GB300 (sm_103a) exact-attention library: the forward
+ * pass (with optional dropout), single-query decode over a dense or paged
+ * cache, the backward pass and a standalone row softmax.
  *
  * The library computes exact scaled-dot-product attention
  *
