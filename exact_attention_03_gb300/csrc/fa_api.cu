@@ -14,8 +14,6 @@ namespace fa {
 // [0] status of the first device-side wait that gave up (0 = none), [1] its site.
 __device__ int g_device_error[2];
 
-namespace {
-
 constexpr int kMaxDevices = 64;
 
 int* error_word_ptr(int dev) {
@@ -30,6 +28,8 @@ int* error_word_ptr(int dev) {
   }
   return cached[dev];
 }
+
+namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -80,6 +80,10 @@ int launch_backward(const void* q, const void* k, const void* v, const void* o, 
 
 int num_sms_of_current_device(int* num_sms);
 
+// The device error word of device `dev` ([0] status, [1] wait site), whose
+// address the library looks up once per device; nullptr on failure.
+int* error_word_ptr(int dev);
+
 // Grid order for work in tiles of whole heads: heads in groups of `group`, all
 // tiles of a group before the next group, so that the CTAs resident at one
 // time share a few heads' K/V (or Q/dO) in L2 instead of streaming every

@@ -1,8 +1,11 @@
 """GPU parity of the two-read row softmax (fa_softmax_rows through the C ABI)
 with the fp64 oracle oracle.softmax, element by element: short rows (one warp
-per row) and long rows (one CTA per row), column counts that are not a
-multiple of 4, single-column rows, in place, masked (-inf) entries and
-all-masked rows, large logits, and a 1 GiB matrix checked on sampled rows."""
+per row), long rows read through shared memory (aligned, a multiple of 4
+columns, up to 16384 of them; several rows per CTA through its two row
+buffers) and the other long rows (one CTA per row from global memory),
+column counts that are not a multiple of 4, unaligned input or output,
+single-column rows, in place, masked (-inf) entries and all-masked rows,
+large logits, and a 1 GiB matrix checked on sampled rows."""
 import numpy as np
 import pytest
 import torch
@@ -42,7 +45,7 @@ def _x(rows, cols, seed, std=3.0):
     return (torch.randn(rows, cols, generator=g) * std).cuda()
 
 
-@pytest.mark.parametrize("cols", [1, 3, 4, 5, 127, 128, 2048, 2049, 3000, 65536])
+@pytest.mark.parametrize("cols", [1, 3, 4, 5, 127, 128, 2048, 2049, 2052, 3000, 16384, 16388, 65536])
 def test_shapes(cols):
     rows = max(1, min(300, (1 << 22) // cols))
     x = _x(rows, cols, cols)
@@ -80,3 +83,33 @@ def test_one_gib_sampled_rows():
                                atol=1e-5, rtol=0)
     del x, y
     torch.cuda.empty_cache()
+
+
+def test_shared_memory_rows_masked_and_many_rows_per_cta():
+    # 2000 rows of 4096 on a few hundred CTAs: each CTA's two buffers cycle
+    # through several phases; masked columns and an all-masked row
+    x = _x(2000, 4096, 11)
+    x[:, ::5] = float("-inf")
+    x[17] = float("-inf")
+    y, lse = fa.softmax_rows(x)
+    _compare(x, y, lse)
+    assert torch.all(y[17] == 0) and torch.isneginf(lse[17])
+
+
+@pytest.mark.parametrize("shift_x,shift_y", [(1, 0), (0, 1), (2, 3)])
+def test_unaligned_input_or_output(shift_x, shift_y):
+    # views starting 4, 8 or 12 bytes into their storage: an unaligned input
+    # takes the global-memory kernel, an unaligned output the scalar stores
+    rows, cols = 300, 4096
+    src = _x(rows, cols, 13)
+    xb = torch.empty(rows * cols + 4, dtype=torch.float32, device="cuda")
+    yb = torch.empty(rows * cols + 4, dtype=torch.float32, device="cuda")
+    x = xb[shift_x:shift_x + rows * cols].view(rows, cols)
+    x.copy_(src)
+    y = yb[shift_y:shift_y + rows * cols].view(rows, cols)
+    out, lse = fa.softmax_rows(x, out=y)
+    _compare(src, out, lse)
+    # the aligned call may take the other kernel, whose sums run in another
+    # order: the two agree within the oracle bound
+    ref, ref_lse = fa.softmax_rows(src)
+    torch.testing.assert_close(out, ref, atol=ATOL_Y, rtol=0)
