@@ -3,7 +3,9 @@ element: the forward (head dims 64 and 128, causal or not, lengths that are
 and are not multiples of the 128-row tiles, Lq != Lk, a custom scale, and
 logits of several magnitudes), the backward, the forward with dropout
 (random p, 64-bit seeds and offsets) and the paged decode (random page
-sizes, lengths, empty sequences, page tables).  The shapes come from one
+sizes, lengths, empty sequences, page tables); and forward cases with many
+heads, whose grids run several waves and walk the heads in L2-sized groups
+with a ragged last group, checked on sampled heads.  The shapes come from one
 fixed generator, so a failure names a reproducible case; they complement the
 hand-picked edge shapes of the other parity tests."""
 import math
@@ -55,6 +57,42 @@ def test_forward_random_shape(i, B, H, Lq, Lk, D, causal, std, scale):
     o, lse = run_gpu(q, k, v, causal, s)
     torch.cuda.synchronize()
     do, dl, n = compare_heads(q, k, v, o, lse, s, causal)
+    assert do <= ATOL_O, f"case {i}: max |dO| = {do:.3e}"
+    assert dl <= ATOL_LSE, f"case {i}: max |dLSE| = {dl:.3e}"
+
+
+def _many_head_cases(n=8, seed=4254):
+    # grids of several waves, heads walked in L2-sized groups with a ragged last
+    # group (24 MB of K/V per group: 8 to 64 heads at these lengths)
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        D = rng.choice((64, 128))
+        causal = rng.random() < 0.5
+        Lq = rng.randint(200, 1600)
+        Lk = Lq if causal else rng.choice((Lq, rng.randint(150, 1600)))
+        B = rng.choice((2, 3, 4))
+        H = rng.choice((5, 12, 17, 24))
+        cases.append((i, B, H, Lq, Lk, D, causal))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,H,Lq,Lk,D,causal", _many_head_cases())
+def test_forward_many_heads(i, B, H, Lq, Lk, D, causal):
+    g = torch.Generator().manual_seed(5000 + i)
+    q = torch.randn(B, H, Lq, D, generator=g).to(torch.bfloat16).cuda()
+    k = torch.randn(B, H, Lk, D, generator=g).to(torch.bfloat16).cuda()
+    v = torch.randn(B, H, Lk, D, generator=g).to(torch.bfloat16).cuda()
+    s = 1.0 / math.sqrt(D)
+    o, lse = run_gpu(q, k, v, causal, s)
+    torch.cuda.synchronize()
+    # the first and last heads, one in the middle and a random one; all rows of
+    # the first, sampled rows (tile boundaries and the last row) of the others
+    rng = random.Random(i)
+    heads = [(0, 0), (B - 1, H - 1), (B // 2, H // 2), (rng.randrange(B), rng.randrange(H))]
+    rows = [None] + [np.unique(np.clip(np.array([0, 127, 128, Lq // 2, Lq - 1] +
+                                                 [rng.randrange(Lq) for _ in range(40)]), 0, Lq - 1))] * 3
+    do, dl, n = compare_heads(q, k, v, o, lse, s, causal, heads=heads, rows=rows)
     assert do <= ATOL_O, f"case {i}: max |dO| = {do:.3e}"
     assert dl <= ATOL_LSE, f"case {i}: max |dLSE| = {dl:.3e}"
 
