@@ -19,8 +19,11 @@
 //    about half an iteration apart (the second starts once the first has its
 //    first half tile of weights), so that one group's TMEM loads, barrier waits
 //    and the drain of its exponentials overlap the other's exponentials.
-//  * Exponentials are taken against the running maximum and checked
-//    afterwards; the row maximum is computed only when the check fails.
+//  * Without dropout, exponentials would be taken against the running
+//    maximum and checked afterwards, the row maximum computed only when the
+//    check fails; with dropout (the only form this file now runs) every tile
+//    takes its row maximum first, since a recomputed tile would draw its
+//    random bits twice.
 //  * K_j and V_j share one ring slot and one "full" barrier (two producer
 //    warps, one TMA box each).
 //
