@@ -36,6 +36,19 @@ So, for one head, in the order of the pages' steps:
     z    = keep mask from the contract above
     O    = ((w * z) @ v) * 256 / (256 - t)
     LSE  = log-sum-exp of a              (unchanged by dropout)
+
+The backward (fa_bwd_dropout) is the gradient of <dO, O> for that forward,
+with the keep mask z fixed (it depends on the seed, not on q, k, v); with
+s = 256 / (256 - t), step by step:
+
+    dV  = s (w * z)^T dO
+    dWz = dO v^T                         gradient of the dropped weights
+    dW  = s z * dWz                      gradient of the weights w
+    dA  = w * (dW - rowsum(w * dW))      softmax's Jacobian
+    dQ  = scale dA k,   dK = scale dA^T q
+
+(rowsum(w * dW) equals rowsum(dO * O) with O the dropout forward's output,
+the quantity FlashAttention-style backward passes compute once per row.)
 """
 from __future__ import annotations
 
@@ -46,7 +59,8 @@ import numpy as np
 from oracle.naive import attention_rows
 from oracle.philox import philox4x32_10
 
-__all__ = ["drop_threshold", "keep_mask", "attention_dropout_rows", "attention_dropout"]
+__all__ = ["drop_threshold", "keep_mask", "attention_dropout_rows", "attention_dropout",
+           "backward_dropout_head", "backward_dropout"]
 
 
 def drop_threshold(p_drop: float) -> int:
@@ -100,3 +114,34 @@ def attention_dropout(q, k, v, scale, causal, p_drop, seed, offset):
             O[b, h], LSE[b, h], _ = attention_dropout_rows(q[b, h], k[b, h], v[b, h], scale, causal, rows,
                                                            b * H + h, p_drop, seed, offset)
     return O, LSE
+
+
+def backward_dropout_head(q, k, v, do, scale, causal, bh, p_drop, seed, offset):
+    """Gradients of <dO, O> for one head of the dropout forward (head index bh
+    in the counter): q, do [Lq, D]; k, v [Lk, D].  Returns dq, dk, dv (fp64)."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    t = drop_threshold(p_drop)
+    s = 256.0 / (256.0 - t)
+    rows = np.arange(q.shape[0])
+    _, _, w = attention_rows(q, k, v, scale, causal=causal, row_index=rows, return_weights=True)
+    z = keep_mask(bh, rows, k.shape[0], t, seed, offset).astype(np.float64)
+    dv = s * ((w * z).T @ do)
+    dwz = do @ v.T
+    dw = s * z * dwz
+    da = w * (dw - (w * dw).sum(axis=1, keepdims=True))
+    dq = float(scale) * (da @ k)
+    dk = float(scale) * (da.T @ q)
+    return dq, dk, dv
+
+
+def backward_dropout(q, k, v, do, scale, causal, p_drop, seed, offset):
+    """[B, H, L, D] inputs (exact widenings of bf16 or fp64).  Returns dq, dk,
+    dv as fp64 arrays of the inputs' shapes.  Meant for small shapes."""
+    q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+    dq, dk, dv = np.empty_like(q), np.empty_like(k), np.empty_like(v)
+    B, H = q.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h] = backward_dropout_head(q[b, h], k[b, h], v[b, h], do[b, h], scale,
+                                                                 causal, b * H + h, p_drop, seed, offset)
+    return dq, dk, dv

@@ -185,3 +185,104 @@ def test_planted_mistakes_fail():
                           np.uint64(0), np.uint64(0)), (1, 0))
     be = np.stack(x, -1).astype(">u4").view(np.uint8).reshape(8, -1)[:, :64] >= t
     assert (be != z).mean() > 0.3
+
+
+# ---------------------------------------------------------------- backward
+
+def _bw_case(seed, Lq=6, Lk=9, D=4):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((Lq, D)), rng.standard_normal((Lk, D)),
+            rng.standard_normal((Lk, D)), rng.standard_normal((Lq, D)))
+
+
+def _dropout_forward(q, k, v, scale, causal, bh, p, seed, offset):
+    o, _, _ = od.attention_dropout_rows(q, k, v, scale, causal, np.arange(q.shape[0]), bh, p, seed, offset)
+    return o
+
+
+def _fd_check(grads, q, k, v, do, scale, causal, bh, p, seed, offset, rng_seed):
+    """Central differences of <dO, O> along random directions, the keep mask
+    fixed by the seed; returns the worst relative mismatch."""
+    f = lambda q_, k_, v_: float((do * _dropout_forward(q_, k_, v_, scale, causal, bh, p, seed, offset)).sum())
+    rng = np.random.default_rng(rng_seed)
+    h = 1e-5
+    worst = 0.0
+    for which, g in zip(("q", "k", "v"), grads):
+        for _ in range(3):
+            u = rng.standard_normal(g.shape)
+            ap = {"q": q, "k": k, "v": v}
+            am = dict(ap)
+            ap[which] = ap[which] + h * u
+            am[which] = am[which] - h * u
+            fd = (f(ap["q"], ap["k"], ap["v"]) - f(am["q"], am["k"], am["v"])) / (2 * h)
+            worst = max(worst, abs(fd - float((g * u).sum())) / max(1.0, abs(fd)))
+    return worst
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("p", [0.3, 0.75])
+def test_backward_finite_differences(causal, p):
+    q, k, v, do = _bw_case(11)
+    if causal:
+        k, v = k[:6], v[:6]
+    scale, bh, seed, offset = 0.7, 5, 0x0123_4567_89AB_CDEF, 9
+    grads = od.backward_dropout_head(q, k, v, do, scale, causal, bh, p, seed, offset)
+    assert _fd_check(grads, q, k, v, do, scale, causal, bh, p, seed, offset, 12) <= 1e-7
+    # the mask matters: at this p some weights are dropped
+    z = od.keep_mask(bh, np.arange(6), k.shape[0], od.drop_threshold(p), seed, offset)
+    assert not z.all()
+
+
+def test_backward_p_zero_is_the_plain_backward():
+    from oracle.backward import backward_head
+    q, k, v, do = _bw_case(13)
+    for causal in (False, True):
+        kk, vv = (k[:6], v[:6]) if causal else (k, v)
+        a = od.backward_dropout_head(q, kk, vv, do, 0.4, causal, 2, 0.0, 1, 0)
+        b = backward_head(q, kk, vv, do, 0.4, causal)
+        for x, y in zip(a, b):
+            np.testing.assert_allclose(x, y, rtol=1e-12, atol=1e-13)
+
+
+def test_backward_row_term_equals_rowsum_do_times_o():
+    # rowsum(w * dW) (the oracle's form) = rowsum(dO * O) with O the dropout
+    # forward's output (the form the kernels compute once per row)
+    q, k, v, do = _bw_case(14)
+    scale, bh, p, seed, offset = 0.5, 1, 0.4, 77, 3
+    t = od.drop_threshold(p)
+    s = 256.0 / (256.0 - t)
+    _, _, w = attention_rows(q, k, v, scale, causal=False, row_index=np.arange(6), return_weights=True)
+    z = od.keep_mask(bh, np.arange(6), k.shape[0], t, seed, offset)
+    dw = s * z * (do @ v.T)
+    o = _dropout_forward(q, k, v, scale, False, bh, p, seed, offset)
+    np.testing.assert_allclose((w * dw).sum(1), (do * o).sum(1), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("kind", ["dV without the mask", "dW without the scale", "row term of undropped weights",
+                                  "mask on dQ only"])
+def test_backward_planted_mistakes_fail_finite_differences(kind):
+    q, k, v, do = _bw_case(15)
+    scale, bh, p, seed, offset = 0.6, 4, 0.5, 2024, 0
+
+    def mutant():
+        t = od.drop_threshold(p)
+        s = 256.0 / (256.0 - t)
+        _, _, w = attention_rows(q, k, v, scale, causal=False, row_index=np.arange(6), return_weights=True)
+        z = od.keep_mask(bh, np.arange(6), k.shape[0], t, seed, offset).astype(float)
+        dv = s * ((w * z).T @ do) if kind != "dV without the mask" else s * (w.T @ do)
+        dwz = do @ v.T
+        dw = s * z * dwz if kind != "dW without the scale" else z * dwz
+        if kind == "row term of undropped weights":
+            da = w * (dw - (w * dwz).sum(1, keepdims=True))
+        else:
+            da = w * (dw - (w * dw).sum(1, keepdims=True))
+        dq = scale * (da @ k)
+        if kind == "mask on dQ only":
+            da2 = w * (dwz - (w * dwz).sum(1, keepdims=True))
+            return dq, scale * (da2.T @ q), dv
+        return dq, scale * (da.T @ q), dv
+
+    assert _fd_check(mutant(), q, k, v, do, scale, False, bh, p, seed, offset, 16) > 1e-3
+    # and the oracle itself passes the same check
+    good = od.backward_dropout_head(q, k, v, do, scale, False, bh, p, seed, offset)
+    assert _fd_check(good, q, k, v, do, scale, False, bh, p, seed, offset, 16) <= 1e-7
