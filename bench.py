@@ -57,10 +57,12 @@ def load_peaks():
 
 
 _CSRC = "exact_attention_03_gb300/csrc/"
-PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d128_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
+PREFILL_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d128_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
+                                            "philox.cuh"))
 PREFILL_D64_SOURCES = tuple(_CSRC + f for f in ("fa_prefill_d64x1_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
 DECODE_SOURCES = tuple(_CSRC + f for f in ("fa_decode_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
-BACKWARD_SOURCES = tuple(_CSRC + f for f in ("fa_backward_sm103.cu", "sm103_ptx.cuh", "fa_internal.h"))
+BACKWARD_SOURCES = tuple(_CSRC + f for f in ("fa_backward_sm103.cu", "sm103_ptx.cuh", "fa_internal.h",
+                                             "philox.cuh"))
 
 
 def measured_traffic(key, sources):
@@ -393,6 +395,23 @@ def per_config_backward(fa, flush, dev, peaks, check):
                                        "frac_bf16_nominal": round(tf / NOMINAL_BF16_TFLOPS, 4),
                                        "launches": 3, "flops_counted": flops,
                                        "traffic": measured_traffic("fa_bwd/causal_l8k_d128", BACKWARD_SOURCES)}
+    # the backward of the dropout forward (fa_bwd_dropout, p = 0.1): the same
+    # products, the keep bits drawn again in both kernels
+    o, lse = fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=True)
+    call = lambda: fa.backward_dropout(q, k, v, o, lse, do, 0.1, 1234, 0, causal=True, dq=dq, dk=dk, dv=dv)
+    _time_launches([call], flush, 2)
+    ts = _time_launches([call], flush, 10)
+    check()
+    ms_d = statistics.median(ts)
+    tf = flops / (ms_d * 1e-3) / 1e12
+    out["backward_dropout_causal_l8k_d128"] = {"B": w.B, "H": w.H, "L": w.Lq, "D": w.D, "causal": True,
+                                               "p_drop": 0.1, "ms": round(ms_d, 5), "TFLOPS": round(tf, 2),
+                                               "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
+                                               "frac_bf16_nominal": round(tf / NOMINAL_BF16_TFLOPS, 4),
+                                               "vs_no_dropout": round(ms_d / ms, 3),
+                                               "launches": 3, "flops_counted": flops,
+                                               "traffic": measured_traffic("fa_bwd_dropout/causal_l8k_d128",
+                                                                           BACKWARD_SOURCES)}
     del q, k, v, do, o, lse, dq, dk, dv
     torch.cuda.empty_cache()
     return out
@@ -655,7 +674,8 @@ def run_reference(args, rank, world):
 def run_profile_case(args):
     """Runs one workload `reps` times with no flush or timing: the command
     the ncu captures profile.  `--profile-op` picks the operation: the
-    forward, the forward with dropout or the backward on a prefill workload,
+    forward, the forward with dropout, the backward or the backward with
+    dropout on a prefill workload,
     the paged decode on a paged workload, or the row softmax (an 8192 x 8192
     fp32 matrix; the case name is ignored)."""
     import dataclasses
@@ -688,6 +708,11 @@ def run_profile_case(args):
             call = lambda: fa.forward(q, k, v, causal=w.causal)
         elif args.profile_op == "dropout":
             call = lambda: fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal)
+        elif args.profile_op == "backward_dropout":
+            g = torch.Generator(device="cuda").manual_seed(11)
+            do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+            o, lse = fa.forward_dropout(q, k, v, 0.1, 1234, 0, causal=w.causal)
+            call = lambda: fa.backward_dropout(q, k, v, o, lse, do, 0.1, 1234, 0, causal=w.causal)
         else:
             g = torch.Generator(device="cuda").manual_seed(11)
             do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
@@ -715,7 +740,8 @@ def main():
                     help="also time the oracle on bounded samples of the other workloads (~20 s)")
     ap.add_argument("--profile-case", default=None, help="run one workload (for ncu captures)")
     ap.add_argument("--profile-batch", type=int, default=0, help="batch override for --profile-case")
-    ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward", "paged", "softmax"],
+    ap.add_argument("--profile-op", default="forward", choices=["forward", "dropout", "backward", "backward_dropout", "paged",
+                                                        "softmax"],
                     help="operation run by --profile-case")
     ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()

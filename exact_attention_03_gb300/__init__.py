@@ -20,7 +20,7 @@ __all__ = ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGN
            "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FlashAttentionError", "lib_path", "load",
            "fa_fwd", "strerror", "last_device_error", "wait_selftest", "decode_num_splits",
            "forward", "forward_host", "decode_noalloc", "decode_paged", "softmax_rows",
-           "backward", "forward_dropout", "EXPORTED_SYMBOLS"]
+           "backward", "backward_dropout", "forward_dropout", "EXPORTED_SYMBOLS"]
 
 FA_OK = 0
 FA_ERR_INVALID_ARG = -1
@@ -59,6 +59,9 @@ _SIGS = {
     "fa_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
                + [ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "fa_fwd_dropout": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
+                       + [ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
+                          ctypes.c_uint, ctypes.c_void_p]),
+    "fa_bwd_dropout": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5
                        + [ctypes.c_float, ctypes.c_int, ctypes.c_float, ctypes.c_ulonglong,
                           ctypes.c_uint, ctypes.c_void_p]),
     "fa_fwd_host": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5
@@ -295,6 +298,20 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     """Gradients (dq, dk, dv) of <dout, O> through fa_bwd, for CUDA bf16
     q, o, dout [B, H, Lq, D], k, v [B, H, Lk, D] and fp32 lse [B, H, Lq] from
     forward() with the same causal flag and scale."""
+    return _backward(q, k, v, o, lse, dout, causal, scale, dq, dk, dv, stream, None)
+
+
+def backward_dropout(q, k, v, o, lse, dout, p_drop: float, seed: int, offset: int = 0,
+                     causal: bool = False, scale: Optional[float] = None, dq=None, dk=None,
+                     dv=None, stream=None):
+    """backward() for forward_dropout() (fa_bwd_dropout): o and lse are
+    forward_dropout's outputs, and p_drop, seed and offset the ones it was
+    called with; the kernels draw the same keep bits again."""
+    return _backward(q, k, v, o, lse, dout, causal, scale, dq, dk, dv, stream,
+                     (float(p_drop), int(seed) & ((1 << 64) - 1), int(offset) & 0xFFFFFFFF))
+
+
+def _backward(q, k, v, o, lse, dout, causal, scale, dq, dk, dv, stream, drop):
     import torch
 
     B, H, Lq, D = q.shape
@@ -310,11 +327,17 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale: Optional[float]
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    st = load().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
-                       lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D,
-                       float(scale), int(causal), _stream_handle(stream))
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D,
+            float(scale), int(causal))
+    if drop is None:
+        name = "fa_bwd"
+        st = load().fa_bwd(*ptrs, _stream_handle(stream))
+    else:
+        name = "fa_bwd_dropout"
+        st = load().fa_bwd_dropout(*ptrs, *drop, _stream_handle(stream))
     if st != FA_OK:
-        raise FlashAttentionError(st, "fa_bwd")
+        raise FlashAttentionError(st, name)
     return dq, dk, dv
 
 

@@ -132,6 +132,22 @@ int launch_prefill(const void* q, const void* k, const void* v, void* o, float* 
   return -2;
 }
 
+// The dropout contract of fa_fwd_dropout / fa_bwd_dropout: t = floor(256 p
+// + 1/2) in double precision (p in [0, 1), t <= 255), keep_scale =
+// 256 / (256 - t), the 64-bit seed split into the Philox key words.
+int make_dropout(float p_drop, unsigned long long seed, unsigned int offset, Dropout* dr) {
+  if (!std::isfinite(p_drop) || !(p_drop >= 0.f) || !(p_drop < 1.f)) return FA_ERR_INVALID_ARG;
+  const double tt = std::floor(double(p_drop) * 256.0 + 0.5);
+  if (tt > 255.0) return FA_ERR_INVALID_ARG;
+  dr->on = 1;
+  dr->seed_lo = uint32_t(seed & 0xffffffffull);
+  dr->seed_hi = uint32_t(seed >> 32);
+  dr->offset = offset;
+  dr->t = uint32_t(tt);
+  dr->keep_scale = float(256.0 / (256.0 - tt));
+  return FA_OK;
+}
+
 int num_sms_of_current_device(int* num_sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -220,9 +236,8 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
   if (B <= 0 || H <= 0 || Lq <= 0 || Lk <= 0 || D <= 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!std::isfinite(p_drop) || !(p_drop >= 0.f) || !(p_drop < 1.f)) return FA_ERR_INVALID_ARG;
-  const double tt = std::floor(double(p_drop) * 256.0 + 0.5);
-  if (tt > 255.0) return FA_ERR_INVALID_ARG;
+  fa::Dropout dr;
+  if (fa::make_dropout(p_drop, seed, offset, &dr) != FA_OK) return FA_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
   if (causal && Lq != Lk) return FA_ERR_UNSUPPORTED;
   const long long BH = (long long)B * H;
@@ -236,13 +251,6 @@ int fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* 
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   int* err = fa::error_word_ptr(dev);
   if (err == nullptr) return FA_ERR_CUDA;
-  fa::Dropout dr;
-  dr.on = 1;
-  dr.seed_lo = uint32_t(seed & 0xffffffffull);
-  dr.seed_hi = uint32_t(seed >> 32);
-  dr.offset = offset;
-  dr.t = uint32_t(tt);
-  dr.keep_scale = float(256.0 / (256.0 - tt));
   return fa::launch_prefill(q, k, v, o, lse, B, H, Lq, Lk, D, scale, causal, s, err, dr);
 }
 
@@ -259,9 +267,13 @@ int fa_last_device_error(void* stream, int* site) {
   return h[0];  // FA_OK, FA_ERR_TIMEOUT, or FA_ERR_INVALID_ARG (a page id out of range)
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int D,
-           float scale, int causal, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_common(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+               void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int D, float scale, int causal,
+               void* stream, const fa::Dropout& dr) {
   // ---- host-side checks, before any CUDA call
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || dout == nullptr ||
       lse == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
@@ -288,11 +300,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
   void* ws = nullptr;
   if (fa::workspace_alloc(&ws, ws_bytes, s) != FA_OK) return FA_ERR_CUDA;
   const int st = fa::launch_backward(q, k, v, o, dout, lse, dq, dk, dv, int(BH), Lq, Lk, D, scale,
-                                     causal, static_cast<float*>(ws), err, s);
+                                     causal, static_cast<float*>(ws), err, s, dr);
   const bool freed = fa::workspace_free(ws, s) == FA_OK;
   if (st == -2) return FA_ERR_UNSUPPORTED;
   if (st != 0) return FA_ERR_CUDA;
   return freed ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int D,
+           float scale, int causal, void* stream) {
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, H, Lq, Lk, D, scale, causal, stream, fa::Dropout());
+}
+
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int D,
+                   float scale, int causal, float p_drop, unsigned long long seed, unsigned int offset,
+                   void* stream) {
+  fa::Dropout dr;
+  if (fa::make_dropout(p_drop, seed, offset, &dr) != FA_OK) return FA_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, dout, lse, dq, dk, dv, B, H, Lq, Lk, D, scale, causal, stream, dr);
 }
 
 int fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache,

@@ -43,6 +43,7 @@
 // double the TMA rate.  Warp 1 = TMEM allocation + MMA issue.
 // Every wait is bounded (the same routine as the forward kernels).
 #include "fa_internal.h"
+#include "philox.cuh"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
@@ -53,7 +54,7 @@ namespace {
 constexpr int kThreads = 352;   // 11 warps
 constexpr float kLog2e = 1.44269504088896340736f;
 
-template <int D, bool DQ>
+template <int D, bool DQ, bool DROP = false>
 struct BwCfg {
   static constexpr int kTileBytes = 128 * D * 2;        // one 128-row tile (one TMA box)
   static constexpr int kSubBytes = 128 * 128;           // one 64-column block of a tile
@@ -65,7 +66,13 @@ struct BwCfg {
   static constexpr int kRingBOff = kRingAOff + kStagesA * kTileBytes;
   static constexpr int kVecOff = kRingBOff + kStagesB * kTileBytes;  // dK/dV: per A stage 128 LSE2 + 128 Dr
   static constexpr int kBarOff = kVecOff + (DQ ? 0 : kStagesA * 1024);
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;
+  // dK/dV with dropout: per element-wise warp, the Philox words of its two
+  // 16-key groups for 64 query rows, [group][word][row], rows padded to 68
+  // words so that the eight rows a warp reads at once fall on different banks
+  static constexpr int kTransRow = 68;
+  static constexpr int kTransWarpBytes = 2 * 4 * kTransRow * 4;
+  static constexpr int kTransOff = kBarOff + 256;
+  static constexpr int kSmemBytes = kTransOff + (DROP && !DQ ? 8 * kTransWarpBytes : 0) + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -79,6 +86,11 @@ struct BwParams {
   int group;              // heads per group of the grid order
   int causal;
   float scale, scale_log2;
+  // dropout (the DROP instantiations): philox.cuh's contract, as in the
+  // forward; keep_scale = 256 / (256 - t)
+  uint32_t seed_lo, seed_hi, offset, drop_tl4, drop_hsel;
+  PhiloxKeys keys;
+  float keep_scale;
 };
 
 // 1-D bulk copy global -> shared, completing `bytes` on `bar` (16-byte aligned, multiple of 16)
@@ -202,6 +214,41 @@ __device__ __forceinline__ void weights_ds(uint32_t tdP, int h, const float (&pv
   }
 }
 
+// With dropout: keep bit of column e from the 16 keep words of a half row
+// (dropout_keep_msb's form: the top bit of byte e mod 4 of word e div 4)
+__device__ __forceinline__ bool keep_bit(const uint32_t (&kw)[16], int e) {
+  return (kw[e >> 2] >> ((e & 3) * 8 + 7)) & 1u;
+}
+
+// the dropped weights p z s of 64 values, bf16 pairs into 32 TMEM columns
+__device__ __forceinline__ void store_packed64_drop(uint32_t taddr, const float (&v)[64], const uint32_t (&kw)[16],
+                                                    float s) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i] * s, v[2 * i + 1] * s) & dropout_pair_mask(kw[i >> 1], i & 1);
+  tmem_st32(taddr, w);
+}
+
+// phase 2 with dropout: dS = p (z s dP - Dr), where dP is the gradient of the
+// dropped weights that the product dO V^T gives
+template <class Dr>
+__device__ __forceinline__ void weights_ds_drop(uint32_t tdP, int h, const float (&pv)[64], Dr dr,
+                                                const uint32_t (&kw)[16], float s) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    float dp[32];
+    tmem_ld32_sync(tdP + 64 * h + 32 * ch, dp);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int e = 32 * ch + 2 * i;
+      const float z0 = keep_bit(kw, e) ? s : 0.f, z1 = keep_bit(kw, e + 1) ? s : 0.f;
+      w[i] = pack_bf16x2(pv[e] * (dp[2 * i] * z0 - dr(e)), pv[e + 1] * (dp[2 * i + 1] * z1 - dr(e + 1)));
+    }
+    tmem_st16(tdP + 64 * h + 16 * ch, w);
+  }
+}
+
 // signal an mbarrier with one arrival per warp once the warp's TMEM stores
 // have completed
 __device__ __forceinline__ void warp_arrive_after_st(uint32_t bar, int lane) {
@@ -224,12 +271,12 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 
 // ---------------------------------------------------------------- dK, dV
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwParams p) {
-  using C = BwCfg<D, false>;
+  using C = BwCfg<D, false, DROP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -374,10 +421,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = uint32_t(g * 32) << 16;
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
     const bool key_ok = key < p.Lk;
+    // dropout: this lane's 16-key group (counter word 0) and its transpose
+    // buffer; the lanes of a group draw the group's words for 4 query rows
+    // each, then each lane reads its key's byte for all 64 rows of the half
+    PhiloxCol pcol;
+    uint32_t* tb = nullptr;
+    if constexpr (DROP) {
+      pcol = philox_col(uint32_t(jt * 8 + g * 2 + (lane >> 4)), uint32_t(bh), p.offset, p.seed_lo, p.seed_hi);
+      tb = reinterpret_cast<uint32_t*>(gbase + C::kTransOff + (warp - 2) * C::kTransWarpBytes);
+    }
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
       const int q0 = (i0 + it) * 128 + 64 * h;
       const bool diag = p.causal && (i0 + it) == jt;
+      uint32_t kw[16];   // dropout: keep bits of this key for the half's 64 query rows
+      if constexpr (DROP) {
+        __syncwarp();    // the previous tile's reads of the buffer are done
+        uint32_t* grp = tb + (lane >> 4) * 4 * C::kTransRow;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int e = (lane & 15) + 16 * t;
+          const uint4 wv = philox4x32_10_col(uint32_t(q0 + e), pcol, p.keys);
+          grp[e] = wv.x;
+          grp[C::kTransRow + e] = wv.y;
+          grp[2 * C::kTransRow + e] = wv.z;
+          grp[3 * C::kTransRow + e] = wv.w;
+        }
+        __syncwarp();
+        // this key's word (j div 4) mod 4 of every row, byte j mod 4 of each
+        const uint4* row = reinterpret_cast<const uint4*>(grp + ((lane & 15) >> 2) * C::kTransRow);
+        const uint32_t sel = uint32_t(lane & 3) | (uint32_t((lane & 3) + 4) << 4);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+          const uint4 w4 = row[m];
+          const uint32_t lo = __byte_perm(w4.x, w4.y, sel), hi = __byte_perm(w4.z, w4.w, sel);
+          kw[m] = dropout_keep_msb(__byte_perm(lo, hi, 0x5410u), p.drop_tl4, p.drop_hsel);
+        }
+      }
       // the stage's LSE2 / Dr slices landed with its Q, dO tiles: wait on that
       // barrier too (already complete; it cannot move on before this tile's
       // products are done) so that the copied values are visible here
@@ -398,12 +478,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         weights_p<false>(pv, p.scale_log2, l2, valid);
       else
         weights_p<true>(pv, p.scale_log2, l2, valid);
-      store_packed64(tS + 64 * h, pv);
+      // dV's operand: the weights as the forward applied them (dropped, scaled)
+      if constexpr (DROP)
+        store_packed64_drop(tS + 64 * h, pv, kw, p.keep_scale);
+      else
+        store_packed64(tS + 64 * h, pv);
       warp_arrive_after_st(bar_P, lane);
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dP, it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
-      weights_ds(tdP, h, pv, [&](int i) { return vdr[i]; });
+      if constexpr (DROP)
+        weights_ds_drop(tdP, h, pv, [&](int i) { return vdr[i]; }, kw, p.keep_scale);
+      else
+        weights_ds(tdP, h, pv, [&](int i) { return vdr[i]; });
       warp_arrive_after_st(bar_dS, lane);
     }
     // epilogue: group 0 writes the dV row of this key, group 1 scale * dK.
@@ -434,12 +521,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- dQ
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwParams p) {
-  using C = BwCfg<D, true>;
+  using C = BwCfg<D, true, DROP>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -567,6 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off, tdP = tmem + lane_off + 128;
     const float l2 = p.lse2[size_t(bh) * p.Lq_pad + qrow];
     const float dr = p.drow[size_t(bh) * p.Lq_pad + qrow];
+    // dropout: the parts of the Philox rounds shared by this row's calls
+    PhiloxRow prow;
+    if constexpr (DROP) prow = philox_row(uint32_t(qrow), uint32_t(bh), p.offset, p.seed_lo, p.seed_hi);
     if (lane == 0) mbar_arrive(ready(0));   // nothing to read before the first tile
     bool ok = true;
     for (int it = 0; it < n && ok; ++it) {
@@ -588,10 +678,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         weights_p<false>(pv, p.scale_log2, l2f, valid);
       else
         weights_p<true>(pv, p.scale_log2, l2f, valid);
+      uint32_t kw[16];   // dropout: keep bits of the half's 64 keys for this row
+      if constexpr (DROP) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 wv = philox4x32_10_row(uint32_t(k0 >> 4) + uint32_t(c), prow, p.keys);
+          kw[4 * c] = dropout_keep_msb(wv.x, p.drop_tl4, p.drop_hsel);
+          kw[4 * c + 1] = dropout_keep_msb(wv.y, p.drop_tl4, p.drop_hsel);
+          kw[4 * c + 2] = dropout_keep_msb(wv.z, p.drop_tl4, p.drop_hsel);
+          kw[4 * c + 3] = dropout_keep_msb(wv.w, p.drop_tl4, p.drop_hsel);
+        }
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(bar_dP, it & 1, abort_flag, p.err, kSiteSoftmaxS));
       if (!ok) break;
       tc_fence_after();
-      weights_ds(tdP, h, pv, [&](int) { return dr; });
+      if constexpr (DROP)
+        weights_ds_drop(tdP, h, pv, [&](int) { return dr; }, kw, p.keep_scale);
+      else
+        weights_ds(tdP, h, pv, [&](int) { return dr; });
       warp_arrive_after_st(bar_dS, lane);
     }
     // epilogue: scale * dQ, columns [h D/2, (h+1) D/2) of this query's row
@@ -617,12 +721,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, float scale,
-                 int causal, float* ws, int* err, cudaStream_t stream) {
-  using CK = BwCfg<D, false>;
-  using CQ = BwCfg<D, true>;
+                 int causal, float* ws, int* err, cudaStream_t stream, const Dropout& dr) {
+  using CK = BwCfg<D, false, DROP>;
+  using CQ = BwCfg<D, true, DROP>;
   CUtensorMap mq, mk, mv, mdo;
   int st = make_tensor_map_bf16(&mq, q, BH, Lq, D);
   if (st == 0) st = make_tensor_map_bf16(&mk, k, BH, Lk, D);
@@ -638,6 +742,13 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   p.err = err;
+  p.seed_lo = dr.seed_lo;
+  p.seed_hi = dr.seed_hi;
+  p.offset = dr.offset;
+  p.drop_tl4 = (dr.t & 0x7fu) * 0x01010101u;
+  p.drop_hsel = dr.t >= 128u ? 0xffffffffu : 0u;
+  p.keys = philox_round_keys(dr.seed_lo, dr.seed_hi);
+  p.keep_scale = dr.keep_scale;
   float* lse2 = ws;
   float* drow = ws + size_t(BH) * p.Lq_pad;
   p.lse2 = lse2;
@@ -651,9 +762,9 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
         BH, Lq, p.Lq_pad);
     if (cudaGetLastError() != cudaSuccess) return -4;
   }
-  if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            CK::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<D, DROP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            CQ::kSmemBytes) != cudaSuccess)
     return -4;
   const long long nk = (long long)((Lk + 127) / 128) * BH;
@@ -662,12 +773,12 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
   p.out_a = static_cast<__nv_bfloat16*>(dk);
   p.out_b = static_cast<__nv_bfloat16*>(dv);
   p.group = l2_head_group(BH, 2ll * Lq * D * 2);   // Q and dO of a head
-  fa_bwd_dkdv_kernel<D><<<dim3(unsigned(nk)), dim3(kThreads), CK::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dkdv_kernel<D, DROP><<<dim3(unsigned(nk)), dim3(kThreads), CK::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   if (cudaGetLastError() != cudaSuccess) return -4;
   p.out_a = static_cast<__nv_bfloat16*>(dq);
   p.out_b = nullptr;
   p.group = l2_head_group(BH, 2ll * Lk * D * 2);   // K and V of a head
-  fa_bwd_dq_kernel<D><<<dim3(unsigned(nq)), dim3(kThreads), CQ::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dq_kernel<D, DROP><<<dim3(unsigned(nq)), dim3(kThreads), CQ::kSmemBytes, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
@@ -675,11 +786,20 @@ int launch_bwd_d(const void* q, const void* k, const void* v, const void* o, con
 
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, int D,
-                    float scale, int causal, float* workspace, int* err, cudaStream_t stream) {
+                    float scale, int causal, float* workspace, int* err, cudaStream_t stream,
+                    const Dropout& dr) {
+  if (D == 64 && dr.on)
+    return launch_bwd_d<64, true>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err,
+                                  stream, dr);
   if (D == 64)
-    return launch_bwd_d<64>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err, stream);
+    return launch_bwd_d<64, false>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err,
+                                   stream, dr);
+  if (D == 128 && dr.on)
+    return launch_bwd_d<128, true>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err,
+                                   stream, dr);
   if (D == 128)
-    return launch_bwd_d<128>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err, stream);
+    return launch_bwd_d<128, false>(q, k, v, o, dout, lse, dq, dk, dv, BH, Lq, Lk, scale, causal, workspace, err,
+                                    stream, dr);
   return -2;
 }
 

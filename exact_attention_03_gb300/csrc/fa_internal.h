@@ -34,6 +34,9 @@ struct Dropout {
   float keep_scale = 1.f;
 };
 
+// The dropout contract from the C ABI's arguments (FA_OK or FA_ERR_INVALID_ARG).
+int make_dropout(float p_drop, unsigned long long seed, unsigned int offset, Dropout* dr);
+
 // Prefill / general path (any Lq, tcgen05 kernel).  Arguments already validated.
 int launch_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                    int Lq, int Lk, int D, float scale, int causal, cudaStream_t stream, int* err,
@@ -74,9 +77,11 @@ int launch_decode_paged(const void* q, const void* k_cache, const void* v_cache,
 
 // Backward pass (fa_bwd): arguments already validated; `workspace` holds
 // 2 * BH * roundup(Lq, 128) floats.  Returns 0, -2 or -4 (or a tensor-map error).
+// With dr.on, the backward of fa_fwd_dropout's forward (the same keep bits).
 int launch_backward(const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, int BH, int Lq, int Lk, int D,
-                    float scale, int causal, float* workspace, int* err, cudaStream_t stream);
+                    float scale, int causal, float* workspace, int* err, cudaStream_t stream,
+                    const Dropout& dr = Dropout());
 
 int num_sms_of_current_device(int* num_sms);
 

@@ -131,6 +131,38 @@ __device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, c
   }
 }
 
+// The column form, for code that walks one key group over many query rows:
+// counter words 0 (j div 16) and 2 (head) and the key are fixed, only word 1
+// (the query row) changes, and round 1 leaves word 1 in word 0 only (xored
+// in).  PhiloxCol holds round 1's result without word 1 and round 2's keys;
+// philox4x32_10_col(i, C, K) returns exactly philox4x32_10((x, i, bh, offset),
+// k0, k1).
+struct PhiloxCol {
+  uint32_t a, b, c, d;   // state after round 1 for row 0 (the row is xored into a)
+  uint32_t k0, k1;       // round 2's keys
+};
+
+__device__ __forceinline__ PhiloxCol philox_col(uint32_t x, uint32_t bh, uint32_t offset, uint32_t k0,
+                                                uint32_t k1) {
+  PhiloxCol C;
+  C.a = __umulhi(0xCD9E8D57u, bh) ^ k0;
+  C.b = 0xCD9E8D57u * bh;
+  C.c = __umulhi(0xD2511F53u, x) ^ offset ^ k1;
+  C.d = 0xD2511F53u * x;
+  C.k0 = k0 + 0x9E3779B9u;
+  C.k1 = k1 + 0xBB67AE85u;
+  return C;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10_col(uint32_t i, const PhiloxCol& C, const PhiloxKeys& K) {
+  uint4 c = make_uint4(C.a ^ i, C.b, C.c, C.d);
+  // round 2
+  const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+  const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+  c = make_uint4(hi1 ^ c.y ^ C.k0, lo1, hi0 ^ c.w ^ C.k1, lo0);
+  return philox_rounds_from_3(c, K);
+}
+
 // The keep decision of four keys at once: byte b of `word` is kept iff
 // b >= t.  With b = 128 h + l and t = 128 ht + lt (h, ht the top bits),
 // z = (word | 0x80808080) - lt * 0x01010101 has in each byte 128 + l - lt,

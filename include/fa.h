@@ -230,6 +230,26 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int D, float scale, int causal, void* stream);
 
 /*
+ * fa_bwd_dropout - backward pass of fa_fwd_dropout: the gradients of
+ * <dout, O> with respect to q, k and v, where O is fa_fwd_dropout's output for
+ * the same q, k, v, scale, causal flag, p_drop, seed and offset.  The keep
+ * bits are drawn again from the same contract (see fa_fwd_dropout), so no
+ * mask is stored between the two passes.  With z the keep mask and
+ * s = 256 / (256 - t):
+ *   dv = s (P * z)^T dout,   dP = s z * (dout v^T),
+ *   dS = P * (dP - rowsum(dout * O)),   dq = scale dS k,   dk = scale dS^T q
+ * (P = exp(scale q k^T - lse); the gradient of a dropped weight is zero).
+ *
+ * Arguments as for fa_bwd (o and lse: fa_fwd_dropout's outputs) and
+ * p_drop, seed, offset as for fa_fwd_dropout; p_drop = 0 gives fa_bwd's
+ * results.  Errors and asynchrony as for fa_fwd.
+ */
+int fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+                   int D, float scale, int causal, float p_drop, unsigned long long seed,
+                   unsigned int offset, void* stream);
+
+/*
  * fa_fwd_dropout - fa_fwd with dropout on the attention weights, fused into the
  * kernel ("6.3 FlashAttention", section "6.3.3 FlashAttention Forward
  * Process", "Kernel Fusion": scale -> mask -> softmax -> dropout -> matrix

@@ -60,6 +60,18 @@ __global__ void philox_probe_row_x2_kernel(const uint32_t* in, uint32_t* out, in
   o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
 }
 
+// the column routine: record i's counter (x, i, bh, offset) through philox_col
+// (x, head, offset and key fixed per column of keys, the query row varying)
+__global__ void philox_probe_col_kernel(const uint32_t* in, uint32_t* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t* r = in + 6 * size_t(i);
+  const fa::PhiloxCol C = fa::philox_col(r[0], r[2], r[3], r[4], r[5]);
+  const uint4 w = fa::philox4x32_10_col(r[1], C, fa::philox_round_keys(r[4], r[5]));
+  uint32_t* o = out + 4 * size_t(i);
+  o[0] = w.x; o[1] = w.y; o[2] = w.z; o[3] = w.w;
+}
+
 // the keep masks of the dropout kernels: record i = (word, t, -, -, -, -);
 // out = (mask of keys 0-1, mask of keys 2-3, -, -)
 __global__ void keep_mask_probe_kernel(const uint32_t* in, uint32_t* out, int n) {
@@ -80,9 +92,10 @@ __global__ void keep_mask_probe_kernel(const uint32_t* in, uint32_t* out, int n)
 // Host buffers in and out; returns 0 or the CUDA error code.  mode: 0 = the
 // single routine, 1 = the paired routine (n even; records 2m, 2m+1 under
 // record 2m's key), 2 = the row routine, 3 = the paired row routine (records
-// 2m, 2m+1 share words 1-3 and the key), 4 = the dropout keep masks.
+// 2m, 2m+1 share words 1-3 and the key), 4 = the dropout keep masks, 5 = the
+// column routine.
 extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int mode) {
-  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 4) return -1;
+  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 5) return -1;
   const bool pairs = (mode == 1 || mode == 3);
   if (pairs && (n & 1)) return -1;
   uint32_t* d_in = nullptr;
@@ -98,6 +111,8 @@ extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, 
       philox_probe_row_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
     else if (mode == 2)
       philox_probe_row_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
+    else if (mode == 5)
+      philox_probe_col_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else if (mode == 4)
       keep_mask_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else

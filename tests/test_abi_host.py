@@ -30,7 +30,7 @@ def test_header_declares_the_expected_entry_points():
     names = declared_functions()
     for n in ("fa_fwd", "fa_strerror", "fa_last_device_error", "fa_decode_num_splits",
               "fa_wait_selftest", "fa_abi_version", "fa_fwd_decode_paged", "fa_softmax_rows",
-              "fa_bwd", "fa_fwd_dropout", "fa_fwd_host", "fa_host_num_chunks",
+              "fa_bwd", "fa_bwd_dropout", "fa_fwd_dropout", "fa_fwd_host", "fa_host_num_chunks",
               "fa_fwd_host_async"):
         assert n in names
 
@@ -214,6 +214,42 @@ def test_bwd_bad_arguments_rejected_on_host(lib, kw, expect):
     a.update(kw)
     assert lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
                       a["B"], a["H"], a["Lq"], a["Lk"], a["D"], a["scale"], a["causal"], None) == expect
+
+
+BWD_DROPOUT_CASES = [
+    (dict(p=-0.1), fa.FA_ERR_INVALID_ARG),
+    (dict(p=1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(p=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(p=0.999), fa.FA_ERR_INVALID_ARG),      # rounds to 256/256
+]
+
+
+@pytest.mark.parametrize("kw,expect", BWD_DROPOUT_CASES + [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=None), fa.FA_ERR_INVALID_ARG),
+    (dict(H=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(D=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(causal=1, Lq=128, Lk=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(do=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_bwd_dropout_bad_arguments_rejected_on_host(lib, kw, expect):
+    a = dict(q=A, k=A, v=A, o=A, do=A, lse=A, dq=A, dk=A, dv=A, B=1, H=1, Lq=128, Lk=128, D=64,
+             scale=0.1, causal=0, p=0.1, seed=(1 << 64) - 1, offset=(1 << 32) - 1)
+    a.update(kw)
+    assert lib.fa_bwd_dropout(a["q"], a["k"], a["v"], a["o"], a["do"], a["lse"], a["dq"], a["dk"], a["dv"],
+                              a["B"], a["H"], a["Lq"], a["Lk"], a["D"], a["scale"], a["causal"], a["p"],
+                              a["seed"], a["offset"], None) == expect
+
+
+def test_bwd_dropout_valid_arguments_without_a_gpu_report_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a GPU (the fake pointers must never reach a kernel)")
+    assert lib.fa_bwd_dropout(A, A, A, A, A, A, A, A, A, 1, 1, 128, 128, 128, 0.1, 1, 0.5, 3, 7,
+                              None) == fa.FA_ERR_CUDA
 
 
 @pytest.mark.parametrize("kw,expect", [

@@ -6,7 +6,8 @@ The oracle's 32-bit Philox is pinned to Triton's independent implementation
 (tests/philox_probe.cu) runs the library's own routines (one counter; two
 counters under one key with their rounds interleaved; and the row forms that
 fold the parts of the first two rounds shared by one query row's calls and
-take the later rounds' keys precomputed) on the same counters and keys, plus
+take the later rounds' keys precomputed, and the column form that folds
+the parts shared by one key block's calls across query rows) on the same counters and keys, plus
 random ones and counters shaped like the dropout contract's, and every output
 word must agree.  The same probe runs the kernels' keep masks (four random
 bytes against the threshold t at once) for every t and every byte value,
@@ -106,6 +107,19 @@ def test_row_device_philox_matches_oracle(probe, paired):
     if paired:
         recs[1::2, 1:] = recs[0::2, 1:]
     assert np.array_equal(_run(probe, recs, mode=3 if paired else 2), _oracle(recs))
+
+
+def test_column_device_philox_matches_oracle(probe):
+    # the column routine of the dropout backward's key-block kernel: word 0
+    # (the key block j div 16), head, offset and key fixed per column, the
+    # query row (word 1) varying
+    rng = np.random.default_rng(9)
+    n = 1 << 14
+    recs = rng.integers(0, 1 << 32, size=(n, 6), dtype=np.uint64)
+    recs[:n // 2, 0] = rng.integers(0, 4096, size=n // 2)
+    recs[:n // 2, 1] = rng.integers(0, 65536, size=n // 2)
+    recs[:n // 2, 2] = rng.integers(0, 512, size=n // 2)
+    assert np.array_equal(_run(probe, recs, mode=5), _oracle(recs))
 
 
 def test_keep_masks_match_the_byte_comparison_for_every_threshold(probe):
