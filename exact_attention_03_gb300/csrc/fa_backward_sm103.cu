@@ -214,23 +214,25 @@ __device__ __forceinline__ void weights_ds(uint32_t tdP, int h, const float (&pv
   }
 }
 
-// With dropout: keep bit of column e from the 16 keep words of a half row
-// (dropout_keep_msb's form: the top bit of byte e mod 4 of word e div 4)
-__device__ __forceinline__ bool keep_bit(const uint32_t (&kw)[16], int e) {
-  return (kw[e >> 2] >> ((e & 3) * 8 + 7)) & 1u;
-}
-
-// the dropped weights p z s of 64 values, bf16 pairs into 32 TMEM columns
-__device__ __forceinline__ void store_packed64_drop(uint32_t taddr, const float (&v)[64], const uint32_t (&kw)[16],
-                                                    float s) {
+// With dropout, the weights dV's product takes: p z (the rescale s is
+// applied to dV once, in the epilogue), bf16 pairs into 32 TMEM columns.
+// kw: the 16 keep words of the 64 values (dropout_keep_msb's form).
+__device__ __forceinline__ void store_packed64_drop(uint32_t taddr, const float (&v)[64], const uint32_t (&kw)[16]) {
   uint32_t w[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i] * s, v[2 * i + 1] * s) & dropout_pair_mask(kw[i >> 1], i & 1);
+  for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]) & dropout_pair_mask(kw[i >> 1], i & 1);
   tmem_st32(taddr, w);
 }
 
-// phase 2 with dropout: dS = p (z s dP - Dr), where dP is the gradient of the
-// dropped weights that the product dO V^T gives
+// dS of one value with dropout: p (s dP - Dr) if kept, else -p Dr, where dP is
+// the gradient of the dropped weight (the product dO V^T gives it).  Written
+// as -p sel(m, Dr - s dP, Dr) with m the key's 32-bit keep mask.
+__device__ __forceinline__ float ds_drop(float p, float dp, float dr, uint32_t m, float s) {
+  const float a = fmaf(-dp, s, dr);
+  return -p * __uint_as_float((__float_as_uint(a) & m) | (__float_as_uint(dr) & ~m));
+}
+
+// phase 2 with dropout: weights_ds with ds_drop per value
 template <class Dr>
 __device__ __forceinline__ void weights_ds_drop(uint32_t tdP, int h, const float (&pv)[64], Dr dr,
                                                 const uint32_t (&kw)[16], float s) {
@@ -242,8 +244,9 @@ __device__ __forceinline__ void weights_ds_drop(uint32_t tdP, int h, const float
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int e = 32 * ch + 2 * i;
-      const float z0 = keep_bit(kw, e) ? s : 0.f, z1 = keep_bit(kw, e + 1) ? s : 0.f;
-      w[i] = pack_bf16x2(pv[e] * (dp[2 * i] * z0 - dr(e)), pv[e + 1] * (dp[2 * i + 1] * z1 - dr(e + 1)));
+      const uint32_t kq = kw[e >> 2];
+      w[i] = pack_bf16x2(ds_drop(pv[e], dp[2 * i], dr(e), dropout_byte_mask(kq, e & 3), s),
+                         ds_drop(pv[e + 1], dp[2 * i + 1], dr(e + 1), dropout_byte_mask(kq, (e + 1) & 3), s));
     }
     tmem_st16(tdP + 64 * h + 16 * ch, w);
   }
@@ -478,9 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         weights_p<false>(pv, p.scale_log2, l2, valid);
       else
         weights_p<true>(pv, p.scale_log2, l2, valid);
-      // dV's operand: the weights as the forward applied them (dropped, scaled)
+      // dV's operand: the weights as the forward applied them (dropped; the
+      // rescale comes in the epilogue)
       if constexpr (DROP)
-        store_packed64_drop(tS + 64 * h, pv, kw, p.keep_scale);
+        store_packed64_drop(tS + 64 * h, pv, kw);
       else
         store_packed64(tS + 64 * h, pv);
       warp_arrive_after_st(bar_P, lane);
@@ -493,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         weights_ds(tdP, h, pv, [&](int i) { return vdr[i]; });
       warp_arrive_after_st(bar_dS, lane);
     }
-    // epilogue: group 0 writes the dV row of this key, group 1 scale * dK.
+    // epilogue: group 0 writes the dV row of this key (times the dropout
+    // rescale s with dropout), group 1 scale * dK.
     // The TMEM loads are warp-collective: every lane takes part, only the
     // stores are predicated.
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag, p.err, kSiteSoftmaxO));
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = key < p.Lk;
       const size_t orow = (size_t(bh) * p.Lk + (valid ? key : 0)) * D;
       __nv_bfloat16* dst = (h == 0 ? p.out_b : p.out_a) + orow;
-      const float mul = h == 0 ? 1.f : p.scale;
+      const float mul = h == 0 ? (DROP ? p.keep_scale : 1.f) : p.scale;
 #pragma unroll 1
       for (int cc = 0; cc < D; cc += 32) {
         float v[32];

@@ -19,11 +19,20 @@
 
 namespace fa {
 
+// The high and low words of the 64-bit product m x, as one wide multiply.
+__device__ __forceinline__ void mul_hi_lo(uint32_t m, uint32_t x, uint32_t& hi, uint32_t& lo) {
+  const unsigned long long pr = (unsigned long long)m * x;
+  hi = uint32_t(pr >> 32);
+  lo = uint32_t(pr);
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    uint32_t hi0, lo0;
+    mul_hi_lo(0xD2511F53u, c.x, hi0, lo0);
+    uint32_t hi1, lo1;
+    mul_hi_lo(0xCD9E8D57u, c.z, hi1, lo1);
     c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
@@ -37,10 +46,14 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 __device__ __forceinline__ void philox4x32_10_x2(uint4& a, uint4& b, uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
-    const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
-    const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
-    const uint32_t bhi1 = __umulhi(0xCD9E8D57u, b.z), blo1 = 0xCD9E8D57u * b.z;
+    uint32_t ahi0, alo0;
+    mul_hi_lo(0xD2511F53u, a.x, ahi0, alo0);
+    uint32_t bhi0, blo0;
+    mul_hi_lo(0xD2511F53u, b.x, bhi0, blo0);
+    uint32_t ahi1, alo1;
+    mul_hi_lo(0xCD9E8D57u, a.z, ahi1, alo1);
+    uint32_t bhi1, blo1;
+    mul_hi_lo(0xCD9E8D57u, b.z, bhi1, blo1);
     a = make_uint4(ahi1 ^ a.y ^ k0, alo1, ahi0 ^ a.w ^ k1, alo0);
     b = make_uint4(bhi1 ^ b.y ^ k0, blo1, bhi0 ^ b.w ^ k1, blo0);
     k0 += 0x9E3779B9u;
@@ -96,8 +109,10 @@ __host__ __device__ inline PhiloxKeys philox_round_keys(uint32_t k0, uint32_t k1
 __device__ __forceinline__ uint4 philox_rounds_from_3(uint4 c, const PhiloxKeys& K) {
 #pragma unroll
   for (int r = 2; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    uint32_t hi0, lo0;
+    mul_hi_lo(0xD2511F53u, c.x, hi0, lo0);
+    uint32_t hi1, lo1;
+    mul_hi_lo(0xCD9E8D57u, c.z, hi1, lo1);
     c = make_uint4(hi1 ^ c.y ^ K.k0[r - 2], lo1, hi0 ^ c.w ^ K.k1[r - 2], lo0);
   }
   return c;
@@ -122,10 +137,14 @@ __device__ __forceinline__ void philox4x32_10_row_x2(uint32_t xa, uint32_t xb, c
 #pragma unroll
   for (int r = 2; r < 10; ++r) {
     const uint32_t kr0 = K.k0[r - 2], kr1 = K.k1[r - 2];
-    const uint32_t ahi0 = __umulhi(0xD2511F53u, a.x), alo0 = 0xD2511F53u * a.x;
-    const uint32_t bhi0 = __umulhi(0xD2511F53u, b.x), blo0 = 0xD2511F53u * b.x;
-    const uint32_t ahi1 = __umulhi(0xCD9E8D57u, a.z), alo1 = 0xCD9E8D57u * a.z;
-    const uint32_t bhi1 = __umulhi(0xCD9E8D57u, b.z), blo1 = 0xCD9E8D57u * b.z;
+    uint32_t ahi0, alo0;
+    mul_hi_lo(0xD2511F53u, a.x, ahi0, alo0);
+    uint32_t bhi0, blo0;
+    mul_hi_lo(0xD2511F53u, b.x, bhi0, blo0);
+    uint32_t ahi1, alo1;
+    mul_hi_lo(0xCD9E8D57u, a.z, ahi1, alo1);
+    uint32_t bhi1, blo1;
+    mul_hi_lo(0xCD9E8D57u, b.z, bhi1, blo1);
     a = make_uint4(ahi1 ^ a.y ^ kr0, alo1, ahi0 ^ a.w ^ kr1, alo0);
     b = make_uint4(bhi1 ^ b.y ^ kr0, blo1, bhi0 ^ b.w ^ kr1, blo0);
   }
@@ -157,8 +176,10 @@ __device__ __forceinline__ PhiloxCol philox_col(uint32_t x, uint32_t bh, uint32_
 __device__ __forceinline__ uint4 philox4x32_10_col(uint32_t i, const PhiloxCol& C, const PhiloxKeys& K) {
   uint4 c = make_uint4(C.a ^ i, C.b, C.c, C.d);
   // round 2
-  const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-  const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+  uint32_t hi0, lo0;
+    mul_hi_lo(0xD2511F53u, c.x, hi0, lo0);
+  uint32_t hi1, lo1;
+    mul_hi_lo(0xCD9E8D57u, c.z, hi1, lo1);
   c = make_uint4(hi1 ^ c.y ^ C.k0, lo1, hi0 ^ c.w ^ C.k1, lo0);
   return philox_rounds_from_3(c, K);
 }
@@ -182,6 +203,15 @@ __host__ __device__ inline uint32_t dropout_keep_msb(uint32_t word, uint32_t tl4
 __device__ __forceinline__ uint32_t dropout_pair_mask(uint32_t keep_msb, int half) {
   uint32_t m;
   asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(keep_msb), "r"(half ? 0xBBAAu : 0x9988u));
+  return m;
+}
+
+// The same keep bits as 32-bit masks, one key at a time: all ones iff the key
+// of byte b (0-3) of a dropout_keep_msb word is kept (the byte's top bit
+// replicated into all four bytes).
+__device__ __forceinline__ uint32_t dropout_byte_mask(uint32_t keep_msb, int b) {
+  uint32_t m;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(m) : "r"(keep_msb), "r"(0x8888u + 0x1111u * uint32_t(b)));
   return m;
 }
 

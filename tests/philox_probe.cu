@@ -87,15 +87,30 @@ __global__ void keep_mask_probe_kernel(const uint32_t* in, uint32_t* out, int n)
   o[3] = 0;
 }
 
+// the per-key keep masks: record i = (word, t, -, -, -, -); out = the 32-bit
+// masks of keys 0, 1, 2, 3
+__global__ void byte_mask_probe_kernel(const uint32_t* in, uint32_t* out, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const uint32_t* r = in + 6 * size_t(i);
+  const uint32_t t = r[1];
+  const uint32_t keep = fa::dropout_keep_msb(r[0], (t & 0x7fu) * 0x01010101u, t >= 128u ? 0xffffffffu : 0u);
+  uint32_t* o = out + 4 * size_t(i);
+  o[0] = fa::dropout_byte_mask(keep, 0);
+  o[1] = fa::dropout_byte_mask(keep, 1);
+  o[2] = fa::dropout_byte_mask(keep, 2);
+  o[3] = fa::dropout_byte_mask(keep, 3);
+}
+
 }  // namespace
 
 // Host buffers in and out; returns 0 or the CUDA error code.  mode: 0 = the
 // single routine, 1 = the paired routine (n even; records 2m, 2m+1 under
 // record 2m's key), 2 = the row routine, 3 = the paired row routine (records
 // 2m, 2m+1 share words 1-3 and the key), 4 = the dropout keep masks, 5 = the
-// column routine.
+// column routine, 6 = the per-key keep masks.
 extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, int mode) {
-  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 5) return -1;
+  if (n <= 0 || in_host == nullptr || out_host == nullptr || mode < 0 || mode > 6) return -1;
   const bool pairs = (mode == 1 || mode == 3);
   if (pairs && (n & 1)) return -1;
   uint32_t* d_in = nullptr;
@@ -111,6 +126,8 @@ extern "C" int philox_probe(const uint32_t* in_host, uint32_t* out_host, int n, 
       philox_probe_row_x2_kernel<<<(n / 2 + 127) / 128, 128>>>(d_in, d_out, n / 2);
     else if (mode == 2)
       philox_probe_row_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
+    else if (mode == 6)
+      byte_mask_probe_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else if (mode == 5)
       philox_probe_col_kernel<<<(n + 127) / 128, 128>>>(d_in, d_out, n);
     else if (mode == 4)

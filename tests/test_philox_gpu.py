@@ -10,8 +10,9 @@ take the later rounds' keys precomputed, and the column form that folds
 the parts shared by one key block's calls across query rows) on the same counters and keys, plus
 random ones and counters shaped like the dropout contract's, and every output
 word must agree.  The same probe runs the kernels' keep masks (four random
-bytes against the threshold t at once) for every t and every byte value,
-against the plain comparison byte >= t.
+bytes against the threshold t at once, as 16-bit pair masks and as 32-bit
+per-key masks) for every t and every byte value, against the plain
+comparison byte >= t.
 """
 import ctypes
 import os
@@ -138,3 +139,7 @@ def test_keep_masks_match_the_byte_comparison_for_every_threshold(probe):
     want_lo = half(keep[0]) | (half(keep[1]) << np.uint32(16))
     want_hi = half(keep[2]) | (half(keep[3]) << np.uint32(16))
     assert np.array_equal(got[:, 0], want_lo) and np.array_equal(got[:, 1], want_hi)
+    # the per-key 32-bit masks of the backward's dS step
+    got = _run(probe, recs, mode=6)
+    for b in range(4):
+        assert np.array_equal(got[:, b], np.where(keep[b], np.uint32(0xffffffff), np.uint32(0)))
