@@ -2,7 +2,7 @@
 element: the forward (head dims 64 and 128, causal or not, lengths that are
 and are not multiples of the 128-row tiles, Lq != Lk, a custom scale, and
 logits of several magnitudes), the backward, the forward with dropout
-(random p, 64-bit seeds and offsets) and the paged decode (random page
+(random p, 64-bit seeds and offsets) and its backward, and the paged decode (random page
 sizes, lengths, empty sequences, page tables); and forward cases with many
 heads, whose grids run several waves and walk the heads in L2-sized groups
 with a ragged last group, checked on sampled heads.  The shapes come from one
@@ -165,6 +165,40 @@ def test_dropout_random_shape(i, B, H, Lq, Lk, D, causal, p, seed64, offset):
             d_l = float(np.abs(to_f64(lse[b, h].cpu()) - rl).max())
             assert d_o <= ATOL_O * 256 / (256 - t), f"case {i}: max |dO| = {d_o:.3e}"
             assert d_l <= ATOL_LSE, f"case {i}: max |dLSE| = {d_l:.3e}"
+
+
+def _dropout_backward_cases(n=8, seed=91):
+    rng = random.Random(seed)
+    cases = []
+    for i in range(n):
+        D = rng.choice((64, 128))
+        causal = rng.random() < 0.5
+        Lq = rng.randint(20, 420)
+        Lk = Lq if causal else rng.randint(20, 420)
+        p = rng.choice((0.05, 0.2, 0.5, 0.9))
+        cases.append((i, rng.choice((1, 2)), rng.choice((1, 2)), Lq, Lk, D, causal, p, rng.getrandbits(64),
+                      rng.getrandbits(32)))
+    return cases
+
+
+@pytest.mark.parametrize("i,B,H,Lq,Lk,D,causal,p,seed64,offset", _dropout_backward_cases())
+def test_dropout_backward_random_shape(i, B, H, Lq, Lk, D, causal, p, seed64, offset):
+    from oracle import dropout as od
+    from oracle.naive import to_f64
+    g = torch.Generator().manual_seed(9000 + i)
+    mk = lambda L: torch.randn(B, H, L, D, generator=g).to(torch.bfloat16).cuda()
+    q, k, v, dout = mk(Lq), mk(Lk), mk(Lk), mk(Lq)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = fa.forward_dropout(q, k, v, p, seed64, offset, causal=causal)
+    dq, dk, dv = fa.backward_dropout(q, k, v, o, lse, dout, p, seed64, offset, causal=causal)
+    st, site = fa.last_device_error()
+    assert st == fa.FA_OK, (st, site)
+    refs = od.backward_dropout(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), to_f64(dout.cpu()), scale,
+                               causal, p, seed64, offset)
+    for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), refs):
+        err = float(np.abs(to_f64(got.cpu()) - ref).max())
+        mag = float(np.abs(ref).max())
+        assert err <= 2e-2 * max(1.0, mag), f"case {i} {name}: {err:.3e} (max |ref| {mag:.3e})"
 
 
 def _paged_cases(n=6, seed=53):
