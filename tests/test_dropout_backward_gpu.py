@@ -16,8 +16,8 @@ CPU from the contract's definition:
     dO is zero outside query block qb (the key-tile kernel's bits again,
     through the dS path);
 * dq, dk, dv element by element for head dims 64 and 128, causal and not,
-  ragged lengths, several key and query tiles, p = 0.1, 0.5, 0.8, 64-bit
-  seeds and offsets;
+  ragged lengths, several key and query tiles, p = 0.1, 0.5, 0.8 (and 0.99),
+  64-bit seeds and offsets, a single query row or key;
 * p = 0 gives fa_bwd's gradients bit for bit;
 * two whole heads of the causal L = 8192 D = 128 workload (slow).
 
@@ -94,6 +94,19 @@ def test_parity_with_oracle(B, H, Lq, Lk, D, causal):
     for p, seed, offset in ((0.1, 5, 0), (0.5, (1 << 40) + 17, 123456), (0.8, 0xFFFF_FFFF_FFFF_FFFF, 0xFFFF_FFFF)):
         got = _grads(q, k, v, do, p, seed, offset, causal)
         _compare(q, k, v, do, got, p, seed, offset, causal)
+
+
+@pytest.mark.parametrize("B,H,Lq,Lk,D,causal,p", [
+    (1, 1, 1, 700, 128, False, 0.5),   # one query row
+    (1, 2, 5, 1, 64, False, 0.5),      # one key
+    (1, 1, 1, 1, 64, False, 0.3),
+    (1, 1, 2, 2, 128, True, 0.5),
+    (1, 2, 200, 333, 64, False, 0.99),  # t = 253: three bytes in 256 kept, s = 256 / 3
+])
+def test_parity_edge_shapes(B, H, Lq, Lk, D, causal, p):
+    q, k, v, do = _inputs(B, H, Lq, Lk, D, seed=Lq * 7 + Lk)
+    got = _grads(q, k, v, do, p, 99, 3, causal)
+    _compare(q, k, v, do, got, p, 99, 3, causal)
 
 
 @pytest.mark.parametrize("D,causal", [(64, False), (128, True)])
