@@ -314,19 +314,25 @@ def backward_dropout(q, k, v, o, lse, dout, p_drop: float, seed: int, offset: in
 def _backward(q, k, v, o, lse, dout, causal, scale, dq, dk, dv, stream, drop):
     import torch
 
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be [B, H, L, D]")
     B, H, Lq, D = q.shape
     Lk = k.shape[2]
-    for name, t, shape in (("q", q, (B, H, Lq, D)), ("k", k, (B, H, Lk, D)), ("v", v, (B, H, Lk, D)),
-                           ("o", o, (B, H, Lq, D)), ("dout", dout, (B, H, Lq, D))):
-        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor of shape {shape}")
-    if tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or not lse.is_cuda:
-        raise ValueError("lse must be a CUDA fp32 tensor [B, H, Lq]")
-    if scale is None:
-        scale = 1.0 / math.sqrt(D)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for name, t, shape in (("q", q, (B, H, Lq, D)), ("k", k, (B, H, Lk, D)), ("v", v, (B, H, Lk, D)),
+                           ("o", o, (B, H, Lq, D)), ("dout", dout, (B, H, Lq, D)),
+                           ("dq", dq, (B, H, Lq, D)), ("dk", dk, (B, H, Lk, D)), ("dv", dv, (B, H, Lk, D))):
+        if tuple(t.shape) != shape or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor of shape {shape}")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
+    if (tuple(lse.shape) != (B, H, Lq) or lse.dtype != torch.float32 or lse.device != q.device
+            or not lse.is_contiguous()):
+        raise ValueError(f"lse must be a contiguous fp32 tensor [B, H, Lq] on {q.device}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
     ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq, Lk, D,
             float(scale), int(causal))

@@ -135,6 +135,13 @@ def test_binding_rejects_bad_tensors(lib):
         fa.forward(q, q, q)  # CPU tensors are refused; no silent fallback
     with pytest.raises(ValueError):
         fa.forward(q[0], q, q)
+    lse = torch.zeros(1, 1, 4)
+    with pytest.raises(ValueError):
+        fa.backward(q, q, q, q, lse, q)
+    with pytest.raises(ValueError):
+        fa.backward_dropout(q, q, q, q, lse, q, 0.1, 1)
+    with pytest.raises(ValueError):
+        fa.backward(q[0], q, q, q, lse, q)
 
 
 def call_paged(**kw):

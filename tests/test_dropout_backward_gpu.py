@@ -215,6 +215,20 @@ def test_invalid_drop_probability_is_rejected():
         assert e.value.status == fa.FA_ERR_INVALID_ARG
 
 
+def test_binding_rejects_bad_gradient_buffers():
+    q, k, v, do = _inputs(1, 2, 128, 256, 64, seed=6)
+    o, lse = fa.forward_dropout(q, k, v, 0.1, 1)
+    for kw in (dict(dq=torch.empty_like(k)), dict(dk=torch.empty_like(q)),
+               dict(dv=torch.empty(v.shape, dtype=torch.float32, device=v.device)),
+               dict(dq=torch.empty_like(q).transpose(2, 3).contiguous().transpose(2, 3))):
+        with pytest.raises(ValueError):
+            fa.backward_dropout(q, k, v, o, lse, do, 0.1, 1, **kw)
+        with pytest.raises(ValueError):
+            fa.backward(q, k, v, o, lse, do, **kw)
+    with pytest.raises(ValueError):
+        fa.backward_dropout(q, k, v, o, lse[:, :, :64], do, 0.1, 1)
+
+
 @pytest.mark.slow
 def test_causal_l8k_d128_whole_heads():
     w = WORKLOADS["causal_l8k_d128"]
