@@ -21,7 +21,17 @@
 //                        S = Q K^T and dP = dO V^T, dS (bf16) over dP, then
 //                        dQ += dS K in TMEM.
 // S and dP are computed twice (once per kernel): no atomics, deterministic
-// results.  TMEM (512 columns): dK/dV kernel S^T [0,128) dP^T [128,256)
+// results.
+// With dropout (the DROP instantiations, the backward of the forward with
+// dropout on the weights): with z the keep mask of philox.cuh's contract and
+// s = 256 / (256 - t), dV = s (P z)^T dO, the weights' gradient is
+// s z dP, and dS = P (s z dP - Dr) (Dr = rowsum(dO * O) with the dropout
+// O); no mask is stored: each kernel draws the bits again.  The dQ kernel's
+// threads own query rows and use the row form of the generator, as the
+// forward does; the dK/dV kernel's threads own keys, so the 16 lanes of a
+// 16-key block draw the block's words for 4 query rows each (the column
+// form) and hand each lane its key's bytes through a per-warp shared-memory
+// transpose.  s multiplies dV once, in the epilogue.  TMEM (512 columns): dK/dV kernel S^T [0,128) dP^T [128,256)
 // dV [256,256+D) dK [256+D,256+2D); dQ kernel S [0,128) dP [128,256)
 // dQ [256,256+D).
 // The element-wise work runs in two phases per tile, each hidden behind two
