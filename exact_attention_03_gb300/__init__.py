@@ -128,6 +128,15 @@ def decode_num_splits(BH: int, Lk: int, num_sms: int) -> int:
     return load().fa_decode_num_splits(int(BH), int(Lk), int(num_sms))
 
 
+def _check_out(name, t, numel, dtype, device):
+    """A caller-supplied output tensor: the C call writes `numel` elements of
+    `dtype` to its data pointer, so it must hold exactly that many,
+    contiguously, on `device` (a torch.device, or "cpu" for host buffers)."""
+    on_device = (not t.is_cuda) if device == "cpu" else (t.is_cuda and t.device == device)
+    if t.numel() != numel or t.dtype != dtype or not t.is_contiguous() or not on_device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of {numel} elements on {device}")
+
+
 def _stream_handle(stream):
     if stream is None:
         import torch
@@ -155,13 +164,19 @@ def forward(q, k, v, causal: bool = False, scale: Optional[float] = None, out=No
             raise ValueError(f"{name} must be a CUDA bf16 tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, device=q.device)
+    else:
+        _check_out("out", out, B * H * Lq * D, torch.bfloat16, q.device)
     if return_lse and lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    elif lse is not None:
+        _check_out("lse", lse, B * H * Lq, torch.float32, q.device)
     st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                 lse.data_ptr() if lse is not None else None, B, H, Lq, Lk, D, scale,
                 int(causal), _stream_handle(stream))
@@ -188,13 +203,19 @@ def forward_dropout(q, k, v, p_drop: float, seed: int, offset: int = 0, causal: 
             raise ValueError(f"{name} must be a CUDA bf16 tensor")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, device=q.device)
+    else:
+        _check_out("out", out, B * H * Lq * D, torch.bfloat16, q.device)
     if lse is None:
         lse = torch.empty((B, H, Lq), dtype=torch.float32, device=q.device)
+    else:
+        _check_out("lse", lse, B * H * Lq, torch.float32, q.device)
     st = load().fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                B, H, Lq, Lk, D, scale, int(causal), float(p_drop),
                                int(seed) & ((1 << 64) - 1), int(offset) & 0xFFFFFFFF,
@@ -282,8 +303,16 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, scale: Optional[flo
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    else:
+        _check_out("out", out, B * H * D, torch.bfloat16, q.device)
     if lse is None:
         lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    else:
+        _check_out("lse", lse, B * H, torch.float32, q.device)
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache), ("block_table", block_table),
+                    ("seq_lens", seq_lens)):
+        if t.device != q.device:
+            raise ValueError(f"{name} is on {t.device}, q on {q.device}")
     st = load().fa_fwd_decode_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
                                     block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
                                     lse.data_ptr(), B, H, D, num_pages, page_size,
@@ -359,8 +388,12 @@ def softmax_rows(x, out=None, lse=None, return_lse: bool = True, stream=None):
     rows = x.numel() // cols if cols > 0 else 0
     if out is None:
         out = torch.empty_like(x)
+    else:
+        _check_out("out", out, x.numel(), torch.float32, x.device)
     if return_lse and lse is None:
         lse = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    elif lse is not None:
+        _check_out("lse", lse, rows, torch.float32, x.device)
     st = load().fa_softmax_rows(x.data_ptr(), out.data_ptr(),
                                 lse.data_ptr() if lse is not None else None, rows, cols,
                                 _stream_handle(stream))
@@ -393,6 +426,10 @@ def forward_host(q, k, v, causal: bool = False, scale: Optional[float] = None, o
     Lk = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
+    if out is not None:
+        _check_out("out", out, B * H * Lq * D, torch.bfloat16, "cpu")
+    if lse is not None:
+        _check_out("lse", lse, B * H * Lq, torch.float32, "cpu")
     if out is None:
         out = torch.empty((B, H, Lq, D), dtype=torch.bfloat16, pin_memory=True)
     if lse is None:

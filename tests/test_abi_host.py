@@ -142,6 +142,14 @@ def test_binding_rejects_bad_tensors(lib):
         fa.backward_dropout(q, q, q, q, lse, q, 0.1, 1)
     with pytest.raises(ValueError):
         fa.backward(q[0], q, q, q, lse, q)
+    # caller-supplied host outputs must hold what the call writes
+    for kw in (dict(out=torch.empty(1, 1, 3, 64, dtype=torch.bfloat16)),
+               dict(out=torch.empty(1, 1, 4, 64, dtype=torch.float32)),
+               dict(out=torch.empty(1, 1, 64, 4, dtype=torch.bfloat16).transpose(2, 3)),
+               dict(lse=torch.empty(1, 1, 5)),
+               dict(lse=torch.empty(1, 1, 4, dtype=torch.float64))):
+        with pytest.raises(ValueError):
+            fa.forward_host(q, q, q, **kw)
 
 
 def call_paged(**kw):
