@@ -1,0 +1,72 @@
+"""Forward passes whose q, k, v and O hold more than 2^31 elements each, so
+that every element offset past the first 2^31 must be computed in 64 bits
+(the TMA coordinates stay per head; the epilogue's O and LSE addresses do
+not).  B = 1, L = 65536, and one head more than 2^31 / (L * D): the last
+head starts at element 2^31 or beyond.  Sampled rows (the first and last of
+the sequence and of a few tiles, plus random ones) of the first, a middle
+and the last head are compared with the fp64 oracle, and at D = 128 the
+forward with dropout too.  About 13 GB on the device per case."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_03_gb300 as fa
+from exact_attention_03_gb300 import build as fa_build
+from exact_attention_03_gb300.inputs import Workload, make_inputs
+from oracle import dropout as od
+from oracle.naive import to_f64
+from parity_util import ATOL_LSE, ATOL_O, compare_heads
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+L = 65536
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    fa_build.build()
+    fa.load()
+    torch.cuda.init()
+
+
+def _rows(seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 32767, 32768, L - 129, L - 128, L - 1]
+    return np.unique(np.concatenate([fixed, rng.choice(L, 12, replace=False)]))
+
+
+def _check():
+    st, site = fa.last_device_error()
+    assert st == fa.FA_OK, f"device wait gave up: status {st} at site {site}"
+
+
+@pytest.mark.parametrize("D,causal", [(128, True), (64, False)])
+def test_forward_beyond_2_31_elements(D, causal):
+    H = (1 << 31) // (L * D) + 1
+    assert H * L * D > (1 << 31) and (H - 1) * L * D >= (1 << 31)
+    w = Workload("max_size", 1, H, L, L, D, causal, seed=7)
+    q, k, v = make_inputs(w, "cuda")
+    o, lse = fa.forward(q, k, v, causal=causal)
+    _check()
+    torch.cuda.synchronize()
+    heads = [(0, 0), (0, H // 2), (0, H - 1)]
+    rows = [_rows(h) for _, h in heads]
+    worst_o, worst_l, n = compare_heads(q, k, v, o, lse, w.scale, causal, heads=heads, rows=rows)
+    print(f"D {D}: {n} rows, max|dO| {worst_o:.3e}, max|dLSE| {worst_l:.3e}")
+    assert worst_o <= ATOL_O and worst_l <= ATOL_LSE
+    if D == 128:
+        p, seed, offset = 0.1, 99, 1
+        del o, lse
+        o, lse = fa.forward_dropout(q, k, v, p, seed, offset, causal=causal)
+        _check()
+        torch.cuda.synchronize()
+        t = od.drop_threshold(p)
+        for (b, h), r in zip(heads, rows):
+            o_ref, lse_ref, _ = od.attention_dropout_rows(to_f64(q[b, h].cpu())[r], to_f64(k[b, h].cpu()),
+                                                          to_f64(v[b, h].cpu()), w.scale, causal, r,
+                                                          b * H + h, p, seed, offset)
+            assert float(np.abs(to_f64(o[b, h].cpu())[r] - o_ref).max()) <= ATOL_O * 256 / (256 - t)
+            assert float(np.abs(to_f64(lse[b, h].cpu())[r] - lse_ref).max()) <= ATOL_LSE
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
