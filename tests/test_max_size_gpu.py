@@ -1,4 +1,4 @@
-"""Forward passes whose q, k, v and O hold more than 2^31 elements each, so
+"""Forward and backward passes whose tensors hold more than 2^31 elements each, so
 that every element offset past the first 2^31 must be computed in 64 bits
 (the TMA coordinates stay per head; the epilogue's O and LSE addresses do
 not).  B = 1, L = 65536, and one head more than 2^31 / (L * D): the last
@@ -69,4 +69,44 @@ def test_forward_beyond_2_31_elements(D, causal):
             assert float(np.abs(to_f64(o[b, h].cpu())[r] - o_ref).max()) <= ATOL_O * 256 / (256 - t)
             assert float(np.abs(to_f64(lse[b, h].cpu())[r] - lse_ref).max()) <= ATOL_LSE
     del q, k, v, o, lse
+    torch.cuda.empty_cache()
+
+
+def test_backward_beyond_2_31_elements_matches_each_head_alone():
+    # the oracle cannot hold a 65536-row head in fp64; heads are independent
+    # and the kernels deterministic, so a head's gradients inside the large
+    # call must equal, bit for bit, those of the same head computed alone (a
+    # wrong offset would read or write another head's rows)
+    D, causal = 128, True
+    H = (1 << 31) // (L * D) + 1
+    w = Workload("max_size_bwd", 1, H, L, L, D, causal, seed=8)
+    q, k, v = make_inputs(w, "cuda")
+    g = torch.Generator(device="cuda").manual_seed(12)
+    do = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    for p_drop in (None, 0.1):
+        if p_drop is None:
+            o, lse = fa.forward(q, k, v, causal=causal)
+            grads = fa.backward(q, k, v, o, lse, do, causal=causal)
+        else:
+            o, lse = fa.forward_dropout(q, k, v, p_drop, 5, 0, causal=causal)
+            grads = fa.backward_dropout(q, k, v, o, lse, do, p_drop, 5, 0, causal=causal)
+        _check()
+        for h in (0, H - 1):
+            sl = lambda t: t[:, h:h + 1].contiguous()
+            if p_drop is None:
+                o1, lse1 = fa.forward(sl(q), sl(k), sl(v), causal=causal)
+                g1 = fa.backward(sl(q), sl(k), sl(v), o1, lse1, sl(do), causal=causal)
+            else:
+                # the keep bits depend on the head's index in its call
+                # (b*H + h), which a one-head call reproduces only for h = 0
+                if h != 0:
+                    continue
+                o1, lse1 = fa.forward_dropout(sl(q), sl(k), sl(v), p_drop, 5, 0, causal=causal)
+                g1 = fa.backward_dropout(sl(q), sl(k), sl(v), o1, lse1, sl(do), p_drop, 5, 0, causal=causal)
+            _check()
+            assert torch.equal(o1, sl(o)) and torch.equal(lse1, sl(lse)), (p_drop, h)
+            for a, b in zip(g1, grads):
+                assert torch.equal(a, sl(b)), (p_drop, h)
+        del o, lse, grads
+    del q, k, v, do
     torch.cuda.empty_cache()
