@@ -1,11 +1,18 @@
-"""Forward and backward passes whose tensors hold more than 2^31 elements each, so
-that every element offset past the first 2^31 must be computed in 64 bits
-(the TMA coordinates stay per head; the epilogue's O and LSE addresses do
-not).  B = 1, L = 65536, and one head more than 2^31 / (L * D): the last
-head starts at element 2^31 or beyond.  Sampled rows (the first and last of
-the sequence and of a few tiles, plus random ones) of the first, a middle
-and the last head are compared with the fp64 oracle, and at D = 128 the
-forward with dropout too.  About 13 GB on the device per case."""
+"""Forward and backward passes whose tensors hold more than 2^31 elements
+each, so that every element offset past the first 2^31 must be computed in
+64 bits (the TMA coordinates stay per head; the epilogues' O, LSE and
+gradient addresses do not).  B = 1, L = 65536, and one head more than
+2^31 / (L * D): the last head starts at element 2^31 or beyond.
+
+* Forward: sampled rows (the first and last of the sequence and of a few
+  tiles, plus random ones) of the first, a middle and the last head against
+  the fp64 oracle, and at D = 128 the forward with dropout too.
+* Backward (D = 128, causal): the oracle cannot hold a 65536-row head, so
+  the first and last heads' outputs and gradients must equal, bit for bit,
+  those of the same head computed alone (plain, and with dropout for head 0,
+  whose index in the keep-bit counter is the same in both calls).
+
+About 13 GB on the device for the forward cases, 35 GB for the backward."""
 import math
 
 import numpy as np
