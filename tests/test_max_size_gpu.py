@@ -12,7 +12,12 @@ gradient addresses do not).  B = 1, L = 65536, and one head more than
   those of the same head computed alone (plain, and with dropout for head 0,
   whose index in the keep-bit counter is the same in both calls).
 
-About 13 GB on the device for the forward cases, 35 GB for the backward."""
+* Row softmax with rows * cols > 2^31, one case per kernel variant (a warp,
+  shared memory or a CTA per row): sampled rows, the last ones included,
+  against the fp64 oracle.
+
+About 13 GB on the device for the forward cases, 35 GB for the backward and
+17 GB for each softmax case."""
 import math
 
 import numpy as np
@@ -116,4 +121,22 @@ def test_backward_beyond_2_31_elements_matches_each_head_alone():
                 assert torch.equal(a, sl(b)), (p_drop, h)
         del o, lse, grads
     del q, k, v, do
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("cols", [1024, 8192, 32768])   # warp, shared-memory and CTA rows
+def test_softmax_rows_beyond_2_31_elements(cols):
+    from oracle.softmax import softmax_rows as oracle_softmax
+    rows = (1 << 31) // cols + 1
+    g = torch.Generator(device="cuda").manual_seed(cols)
+    x = torch.randn(rows, cols, generator=g, device="cuda") * 4
+    y, lse = fa.softmax_rows(x)
+    torch.cuda.synchronize()
+    pick = torch.tensor(sorted({0, 1, rows // 2, rows - 2, rows - 1}
+                               | set(np.random.default_rng(cols).choice(rows, 8, replace=False).tolist())),
+                        device="cuda")
+    ry, rl = oracle_softmax(x[pick].cpu().numpy())
+    assert np.abs(y[pick].cpu().numpy().astype(np.float64) - ry).max() <= 2e-6
+    assert np.abs(lse[pick].cpu().numpy().astype(np.float64) - rl).max() <= 1e-5 * max(1.0, np.abs(rl).max())
+    del x, y, lse
     torch.cuda.empty_cache()
