@@ -64,10 +64,11 @@ namespace {
 constexpr int kThreads = 352;   // 11 warps
 constexpr float kLog2e = 1.44269504088896340736f;
 
+constexpr int kSubBytes = 128 * 128;   // one 64-column block of a 128-row tile
+
 template <int D, bool DQ, bool DROP = false>
 struct BwCfg {
   static constexpr int kTileBytes = 128 * D * 2;        // one 128-row tile (one TMA box)
-  static constexpr int kSubBytes = 128 * 128;           // one 64-column block of a tile
   // ring A: Q tiles (dK/dV kernel) or K tiles (dQ kernel); ring B: dO or V tiles
   static constexpr int kStagesA = D == 64 ? 4 : (DQ ? 3 : 2);
   static constexpr int kStagesB = D == 64 ? 4 : 2;
@@ -171,11 +172,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* o
 template <int D>
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
   constexpr uint64_t kDesc = sdesc_sw128(0, 16, 1024);
-  return sdesc_at(kDesc, tile + (kk >> 2) * BwCfg<D, false>::kSubBytes + (kk & 3) * 32);
+  return sdesc_at(kDesc, tile + (kk >> 2) * kSubBytes + (kk & 3) * 32);
 }
 template <int D>
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int kk) {
-  constexpr uint64_t kDesc = sdesc_sw128(0, BwCfg<D, false>::kSubBytes, 1024);
+  constexpr uint64_t kDesc = sdesc_sw128(0, kSubBytes, 1024);
   return sdesc_at(kDesc, tile + kk * 16 * 128);
 }
 

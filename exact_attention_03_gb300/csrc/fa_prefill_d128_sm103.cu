@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 nm2;
       // 16 pairs of weights of keys 32cb .. 32cb+31, packed to bf16, summed into acc
       auto exp_block = [&](int cb, uint32_t (&w)[16]) {
-        uint4 dw, dw2;     // dropout bits of the block's two groups of 16 keys
-        uint32_t keep4;    // keep bits (byte top bits) of the current 4 keys
+        [[maybe_unused]] uint4 dw, dw2;   // dropout bits of the block's two groups of 16 keys
+        [[maybe_unused]] uint32_t keep4;  // keep bits (byte top bits) of the current 4 keys
         if constexpr (DROP) {
           const uint32_t g16 = uint32_t(j * 128 + 32 * cb) >> 4;
           philox4x32_10_row_x2(g16, g16 + 1u, prow, p.keys, dw, dw2);
